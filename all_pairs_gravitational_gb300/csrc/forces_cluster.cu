@@ -1,0 +1,295 @@
+// forces_cluster.cu -- all-pairs softened gravity for small N: the source
+// range of one target block is split across the warps of a CTA and across
+// the CTAs of a thread-block cluster, and the partial sums are added back in
+// a fixed order through shared memory and distributed shared memory (DSMEM).
+//
+// With one thread per target, N = 1024 bodies would occupy a few SMs of 152
+// (the GPU Gems 3 ch.31 study page, section 4, splits a body's row over
+// several threads below about 4096 bodies and merges the partial
+// accelerations).  Here a cluster of C CTAs shares one block of BI = 32 K
+// targets; CTA c takes source tiles [c T, c T + T) and warp w of it takes
+// the w-th slice of every tile, so C * W pieces of the source range run in
+// parallel, for N * BI / (C * W) pairs each.
+//
+// Reduction, deterministic and without atomics or global scratch:
+//   1. each warp folds its fp32 partials into Kahan totals (as in the tiled
+//      kernel) and writes them to shared memory;
+//   2. the CTA adds its W warp partials in the order w = 0 .. W-1;
+//   3. after a cluster barrier, CTA c adds slice c of the targets over the C
+//      CTAs' shared memory, rank 0 .. C-1, and stores the result;
+//   4. a second cluster barrier keeps every CTA's shared memory alive until
+//      the other CTAs have read it.
+// Tiles are staged exactly as in forces_tiled.cu (cp.async, duplicated
+// layout, zero-filled tail); the pair arithmetic is the same.
+#include <algorithm>
+
+#include "nbody_device.cuh"
+#include "nbody_internal.h"
+
+namespace nbody {
+
+namespace {
+
+constexpr int kStages = 3;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Load a float4 from the shared memory of CTA `rank` of this cluster, at the
+// offset `local` has in this CTA's shared memory.
+__device__ __forceinline__ float4 ld_dsmem_f4(const void *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
+    return v;
+}
+
+template <int NT, int P>
+__device__ __forceinline__ void stage_tile(float *sbuf, const float *pm, int n, int tile) {
+    static_assert((8 * P) % NT == 0, "tile copies must divide evenly among threads");
+    const uint32_t sbase = smem_u32(sbuf);
+    const int64_t j0 = static_cast<int64_t>(tile) * P;
+#pragma unroll
+    for (int r = 0; r < (8 * P) / NT; ++r) {
+        const int idx = r * NT + static_cast<int>(threadIdx.x);
+        const int64_t j = j0 + (idx >> 3);
+        const int comp = (idx >> 1) & 3;
+        const bool ok = j < n;
+        const float *src = pm + (ok ? j * 4 + comp : 0);
+        cp_async_4(sbase + 4u * static_cast<uint32_t>(idx), src, ok ? 4 : 0);
+    }
+}
+
+__device__ __forceinline__ void kahan1(float &hi, float &lo, float x) {
+    const float y = __fsub_rn(x, lo);
+    const float t = __fadd_rn(hi, y);
+    lo = __fsub_rn(__fsub_rn(t, hi), y);
+    hi = t;
+}
+
+template <int K, int W, int P, bool POT>
+__global__ void __launch_bounds__(W * 32)
+forces_cluster_kernel(const float *__restrict__ pm, int n, float eps2, int tiles_per_cta,
+                      int ntiles, float4 *__restrict__ out) {
+    static_assert(K % 2 == 0, "targets are processed in f32x2 pairs");
+    constexpr int KP = K / 2;
+    constexpr int NT = W * 32;
+    constexpr int BI = 32 * K;          // targets per cluster
+    constexpr int JW = P / W;           // sources per warp per tile
+    constexpr int FOLD_P = 8;           // tiles between folds of the potential
+    static_assert(P % W == 0 && JW <= 32, "tile must split evenly, <= 32 sources per warp");
+
+    __shared__ __align__(16) float sdup[kStages][P * 8];
+    __shared__ __align__(16) float4 red[W][BI];
+
+    const int tid = static_cast<int>(threadIdx.x);
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t csize = cluster_nctarank();
+    const int ib = static_cast<int>(blockIdx.x / csize);
+    const int t_begin = static_cast<int>(crank) * tiles_per_cta;
+    const int t_end = min(t_begin + tiles_per_cta, ntiles);
+    const int64_t ibase = static_cast<int64_t>(ib) * BI + lane;
+    const float4 *pm4 = reinterpret_cast<const float4 *>(pm);
+
+    f2 xi[KP], yi[KP], zi[KP];
+#pragma unroll
+    for (int q = 0; q < KP; ++q) {
+        const int64_t i0 = min(ibase + (2 * q) * 32, static_cast<int64_t>(n) - 1);
+        const int64_t i1 = min(ibase + (2 * q + 1) * 32, static_cast<int64_t>(n) - 1);
+        const float4 b0 = __ldg(pm4 + i0);
+        const float4 b1 = __ldg(pm4 + i1);
+        xi[q] = f2_pack(b0.x, b1.x);
+        yi[q] = f2_pack(b0.y, b1.y);
+        zi[q] = f2_pack(b0.z, b1.z);
+    }
+    const f2 e2 = f2_pack(eps2, eps2);
+
+    f2 ax[KP], ay[KP], az[KP], pp[KP];
+    f2 hx[KP], hy[KP], hz[KP], hp[KP];
+    f2 lx[KP], ly[KP], lz[KP], lp[KP];
+#pragma unroll
+    for (int q = 0; q < KP; ++q) {
+        ax[q] = ay[q] = az[q] = pp[q] = 0ull;
+        hx[q] = hy[q] = hz[q] = hp[q] = 0ull;
+        lx[q] = ly[q] = lz[q] = lp[q] = 0ull;
+    }
+
+    if (t_begin < t_end) stage_tile<NT, P>(sdup[0], pm, n, t_begin);
+    cp_async_commit();
+    if (t_begin + 1 < t_end) stage_tile<NT, P>(sdup[1], pm, n, t_begin + 1);
+    cp_async_commit();
+
+    int stage = 0;
+    for (int t = t_begin; t < t_end; ++t) {
+        const int k = t - t_begin;
+        cp_async_wait<1>();
+        __syncthreads();
+        {
+            int s2 = stage + 2;
+            if (s2 >= kStages) s2 -= kStages;
+            if (t + 2 < t_end) stage_tile<NT, P>(sdup[s2], pm, n, t + 2);
+            cp_async_commit();
+        }
+        const float4 *s4 = reinterpret_cast<const float4 *>(sdup[stage]) + 2 * (warp * JW);
+#pragma unroll 4
+        for (int jj = 0; jj < JW; ++jj) {
+            const float4 a = s4[2 * jj];
+            const float4 b = s4[2 * jj + 1];
+            const f2 xj = f2_pack(a.x, a.y);
+            const f2 yj = f2_pack(a.z, a.w);
+            const f2 zj = f2_pack(b.x, b.y);
+            const f2 mj = f2_pack(b.z, b.w);
+#pragma unroll
+            for (int q = 0; q < KP; ++q) {
+                const f2 dx = f2_sub(xj, xi[q]);
+                const f2 dy = f2_sub(yj, yi[q]);
+                const f2 dz = f2_sub(zj, zi[q]);
+                f2 d2 = f2_fma(dx, dx, e2);
+                d2 = f2_fma(dy, dy, d2);
+                d2 = f2_fma(dz, dz, d2);
+                float d2a, d2b;
+                f2_unpack(d2, d2a, d2b);
+                const f2 inv = f2_pack(rsqrt_hw(d2a), rsqrt_hw(d2b));
+                const f2 tm = f2_mul(mj, inv);
+                const f2 inv2 = f2_mul(inv, inv);
+                const f2 s = f2_mul(tm, inv2);
+                ax[q] = f2_fma(s, dx, ax[q]);
+                ay[q] = f2_fma(s, dy, ay[q]);
+                az[q] = f2_fma(s, dz, az[q]);
+                if (POT) pp[q] = f2_add(pp[q], tm);
+            }
+        }
+        // acceleration: fold after every warp slice (<= 32 sources, see
+        // forces_tiled.cu); potential: every FOLD_P tiles
+#pragma unroll
+        for (int q = 0; q < KP; ++q) {
+            f2_kahan_fold(hx[q], lx[q], ax[q]);
+            f2_kahan_fold(hy[q], ly[q], ay[q]);
+            f2_kahan_fold(hz[q], lz[q], az[q]);
+        }
+        if (POT && ((k + 1) % FOLD_P == 0 || t + 1 == t_end)) {
+#pragma unroll
+            for (int q = 0; q < KP; ++q) f2_kahan_fold(hp[q], lp[q], pp[q]);
+        }
+        stage = (stage + 1 == kStages) ? 0 : stage + 1;
+    }
+    cp_async_wait<0>();
+
+    // 1. warp partials to shared memory: slot k*32 + lane is target ib*BI + slot
+#pragma unroll
+    for (int q = 0; q < KP; ++q) {
+        float x0, x1, y0, y1, z0, z1, p0 = 0.f, p1 = 0.f;
+        f2_unpack(f2_sub(hx[q], lx[q]), x0, x1);
+        f2_unpack(f2_sub(hy[q], ly[q]), y0, y1);
+        f2_unpack(f2_sub(hz[q], lz[q]), z0, z1);
+        if (POT) f2_unpack(f2_sub(hp[q], lp[q]), p0, p1);
+        red[warp][(2 * q) * 32 + lane] = make_float4(x0, y0, z0, p0);
+        red[warp][(2 * q + 1) * 32 + lane] = make_float4(x1, y1, z1, p1);
+    }
+    __syncthreads();
+
+    // 2. CTA partial over warps w = 0 .. W-1, in place in red[0]
+    for (int slot = tid; slot < BI; slot += NT) {
+        float4 h = red[0][slot];
+        float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 1; w < W; ++w) {
+            const float4 v = red[w][slot];
+            kahan1(h.x, c.x, v.x);
+            kahan1(h.y, c.y, v.y);
+            kahan1(h.z, c.z, v.z);
+            kahan1(h.w, c.w, v.w);
+        }
+        red[0][slot] = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y),
+                                   __fsub_rn(h.z, c.z), __fsub_rn(h.w, c.w));
+    }
+
+    // 3. cluster partial over ranks 0 .. C-1 for this CTA's slice of targets
+    cluster_sync();
+    const int per = BI / static_cast<int>(csize);
+    for (int t = tid; t < per; t += NT) {
+        const int slot = static_cast<int>(crank) * per + t;
+        float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 c = h;
+        for (uint32_t r = 0; r < csize; ++r) {
+            const float4 v = ld_dsmem_f4(&red[0][slot], r);
+            kahan1(h.x, c.x, v.x);
+            kahan1(h.y, c.y, v.y);
+            kahan1(h.z, c.z, v.z);
+            kahan1(h.w, c.w, v.w);
+        }
+        const int64_t i = static_cast<int64_t>(ib) * BI + slot;
+        if (i < n)
+            out[i] = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y), __fsub_rn(h.z, c.z),
+                                 -__fsub_rn(h.w, c.w));
+    }
+    // 4. keep this CTA's shared memory alive until every rank has read it
+    cluster_sync();
+}
+
+#define NBODY_CLUSTER(K, W, P) {K, W, P, reinterpret_cast<const void *>(&forces_cluster_kernel<K, W, P, true>)}
+
+const ClusterVariant kVariants[] = {
+    NBODY_CLUSTER(2, 4, 128),   // 0: default
+    NBODY_CLUSTER(4, 4, 128),   // 1
+    NBODY_CLUSTER(2, 8, 128),   // 2
+    NBODY_CLUSTER(4, 8, 128),   // 3
+};
+
+#undef NBODY_CLUSTER
+
+template <int K, int W, int P>
+cudaError_t launch_variant(const float *pm, int n, float eps2, int num_ib, int cluster, int tpc,
+                           int ntiles, float4 *out, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_ib) * static_cast<unsigned>(cluster), 1, 1);
+    cfg.blockDim = dim3(W * 32, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true>, pm, n, eps2, tpc, ntiles,
+                              out);
+}
+
+}  // namespace
+
+int cluster_variant_count() { return static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0])); }
+
+const ClusterVariant &cluster_variant(int v) { return kVariants[v]; }
+
+cudaError_t launch_cluster(int variant, const float *pm, int n, float eps2, int num_ib, int cluster,
+                           int tiles_per_cta, int ntiles, float4 *out, cudaStream_t stream) {
+    switch (variant) {
+        case 0: return launch_variant<2, 4, 128>(pm, n, eps2, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        case 1: return launch_variant<4, 4, 128>(pm, n, eps2, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        case 2: return launch_variant<2, 8, 128>(pm, n, eps2, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        case 3: return launch_variant<4, 8, 128>(pm, n, eps2, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace nbody

@@ -1,0 +1,349 @@
+// nbody_api.cu -- the C ABI: argument checks, the launch planner, per-device
+// state and dispatch.  See include/nbody.h for the contract of each call.
+#include <cfloat>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "nbody.h"
+#include "nbody_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+nbody_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return NBODY_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- host checks
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void *a, const void *b, int64_t bytes) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a);
+    const uintptr_t y = reinterpret_cast<uintptr_t>(b);
+    const uintptr_t len = static_cast<uintptr_t>(bytes);
+    return x < y + len && y < x + len;
+}
+
+nbody_status check_n(int64_t n) {
+    return (n < 0 || n > INT32_MAX) ? NBODY_ERR_INVALID_ARG : NBODY_OK;
+}
+
+nbody_status check_forces(const float *pm, int64_t n, float eps2, const float *acc) {
+    if (check_n(n) != NBODY_OK) return NBODY_ERR_INVALID_ARG;
+    if (n == 0) return NBODY_OK;
+    if (pm == nullptr || acc == nullptr) return NBODY_ERR_INVALID_ARG;
+    if (!std::isfinite(eps2) || !(eps2 >= FLT_MIN)) return NBODY_ERR_INVALID_ARG;
+    if (!aligned16(pm) || !aligned16(acc)) return NBODY_ERR_MISALIGNED;
+    if (overlap(pm, acc, 16 * n)) return NBODY_ERR_ALIAS;
+    return NBODY_OK;
+}
+
+// ---------------------------------------------------------------- per-device state
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    int tiled_occ[8] = {0};
+    int cluster_occ[8] = {0};
+    cudaMemPool_t pool = nullptr;     // stream-ordered scratch for split partials
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+nbody_status device_state(DeviceState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return NBODY_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if (major != 10 || minor != 3) return NBODY_ERR_DEVICE;   // built for sm_103a only
+        for (int v = 0; v < nbody::tiled_variant_count() && v < 8; ++v) {
+            const nbody::TiledVariant &tv = nbody::tiled_variant(v);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.tiled_occ[v], tv.fn_pot,
+                                                              tv.threads, 0);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        for (int v = 0; v < nbody::cluster_variant_count() && v < 8; ++v) {
+            const nbody::ClusterVariant &cv = nbody::cluster_variant(v);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.cluster_occ[v], cv.fn_pot,
+                                                              cv.warps * 32, 0);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if ((e = cudaMemPoolCreate(&d.pool, &props)) != cudaSuccess) return cuda_fail(e);
+        uint64_t keep = UINT64_MAX;   // keep freed blocks for the next call
+        if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
+            return cuda_fail(e);
+        d.ready = true;
+    }
+    *out = &d;
+    return NBODY_OK;
+}
+
+// ---------------------------------------------------------------- planner
+
+constexpr int kDefaultTiledVariant = 0;
+constexpr int kMaxSplits = 256;
+constexpr int64_t kMaxScratchBytes = int64_t(2) << 30;
+// Relative cost model (only ratios matter): pair rate of one SM, the fixed
+// cost of a work item in source-body equivalents, one launch, scratch traffic.
+constexpr double kPairsPerSmSecond = 1.4e10;
+constexpr int kItemOverheadBodies = 96;
+constexpr double kLaunchSeconds = 2.5e-6;
+constexpr double kScratchBytesPerSecond = 5.0e12;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+void plan_tiled(int64_t n, int sm, int occ, int variant, int splits_req, nbody_plan *p) {
+    const nbody::TiledVariant &v = nbody::tiled_variant(variant);
+    const int64_t bi = static_cast<int64_t>(v.threads) * v.i_per_thread;
+    const int64_t num_ib = ceil_div(n, bi);
+    const int64_t ntiles = ceil_div(n, v.tile);
+    const int64_t slots = static_cast<int64_t>(sm > 0 ? sm : 1) * (occ > 0 ? occ : 1);
+    const double slot_rate = kPairsPerSmSecond / (occ > 0 ? occ : 1);
+
+    int64_t s_lo = 1, s_hi = std::min<int64_t>(ntiles, kMaxSplits);
+    s_hi = std::max<int64_t>(1, std::min<int64_t>(s_hi, kMaxScratchBytes / (16 * n)));
+    if (splits_req > 0) s_lo = s_hi = std::min<int64_t>(splits_req, ntiles);
+
+    double best_t = INFINITY;
+    int64_t best_s = 1, best_tps = ntiles, best_waves = 1;
+    for (int64_t s = s_lo; s <= s_hi; ++s) {
+        const int64_t tps = ceil_div(ntiles, s);
+        const int64_t used = ceil_div(ntiles, tps);
+        if (used != s && splits_req <= 0) continue;   // same as a smaller S
+        const int64_t items = num_ib * used;
+        const int64_t waves = ceil_div(items, slots);
+        double t = static_cast<double>(waves) *
+                   static_cast<double>(tps * v.tile + kItemOverheadBodies) * bi / slot_rate;
+        if (used > 1) t += kLaunchSeconds + 32.0 * used * n / kScratchBytesPerSecond;
+        if (t < best_t * (1.0 - 1e-3)) {
+            best_t = t;
+            best_s = used;
+            best_tps = tps;
+            best_waves = waves;
+        }
+    }
+    p->path = NBODY_PATH_TILED;
+    p->variant = variant;
+    p->i_per_thread = v.i_per_thread;
+    p->threads = v.threads;
+    p->tile = v.tile;
+    p->num_iblocks = static_cast<int32_t>(num_ib);
+    p->splits = static_cast<int32_t>(best_s);
+    p->tiles_per_split = static_cast<int32_t>(best_tps);
+    p->cluster = 1;
+    p->warps_j = 1;
+    p->grid = num_ib * best_s;
+    p->scratch_bytes = best_s > 1 ? 16 * best_s * n : 0;
+    p->fill = static_cast<double>(num_ib * best_s) / static_cast<double>(best_waves * slots);
+}
+
+// Small-N path: a cluster of C CTAs (C in 1, 2, 4, 8) shares 32 K targets;
+// each CTA has W warps.  Cost model: the busiest SM holds ceil(CTAs / SMs)
+// CTAs (waves beyond the occupancy limit are counted), and an SM reaches its
+// full pair rate with kWarpsToSaturate resident warps.
+constexpr int kWarpsToSaturate = 16;
+
+void plan_cluster_variant(int64_t n, int sm, int occ, int variant, nbody_plan *p, double *t_out) {
+    const nbody::ClusterVariant &v = nbody::cluster_variant(variant);
+    const int64_t bi = 32LL * v.i_per_thread;
+    const int64_t num_ib = ceil_div(n, bi);
+    const int64_t ntiles = ceil_div(n, v.tile);
+    double best_t = INFINITY;
+    int64_t best_c = 1, best_tpc = ntiles;
+    double best_fill = 0.0;
+    for (int64_t c = 1; c <= 8; c *= 2) {
+        if (c > ntiles) break;
+        const int64_t tpc = ceil_div(ntiles, c);
+        const int64_t ctas = num_ib * c;
+        const int64_t per_sm = ceil_div(ctas, sm);
+        const int64_t resident = std::min<int64_t>(per_sm, occ > 0 ? occ : 1);
+        const int64_t waves = ceil_div(per_sm, resident);
+        const double rate = kPairsPerSmSecond *
+                            std::min(1.0, static_cast<double>(resident * v.warps) / kWarpsToSaturate);
+        const double cta_pairs = static_cast<double>(tpc * v.tile + kItemOverheadBodies) * bi;
+        const double t = waves * resident * cta_pairs / rate + 0.2e-6 * (c > 1);
+        if (t < best_t * (1.0 - 1e-3)) {
+            best_t = t;
+            best_c = c;
+            best_tpc = tpc;
+            best_fill = static_cast<double>(ctas) / static_cast<double>(waves * resident * sm);
+        }
+    }
+    p->path = NBODY_PATH_CLUSTER;
+    p->variant = variant;
+    p->i_per_thread = v.i_per_thread;
+    p->threads = v.warps * 32;
+    p->tile = v.tile;
+    p->num_iblocks = static_cast<int32_t>(num_ib);
+    p->splits = static_cast<int32_t>(best_c * v.warps);
+    p->tiles_per_split = static_cast<int32_t>(best_tpc);
+    p->cluster = static_cast<int32_t>(best_c);
+    p->warps_j = v.warps;
+    p->grid = num_ib * best_c;
+    p->scratch_bytes = 0;
+    p->fill = best_fill > 1.0 ? 1.0 : best_fill;
+    *t_out = best_t;
+}
+
+// Largest n the automatic choice sends to the cluster path (measured on
+// GB300: the cluster path is ahead up to 8192 bodies, the tiled one from 12288).
+constexpr int64_t kClusterMaxN = 10240;
+
+nbody_status make_plan(int64_t n, int sm, const int *tiled_occ, const int *cluster_occ,
+                       const nbody_forces_opts *opts, nbody_plan *p) {
+    if (n <= 0 || n > INT32_MAX || sm <= 0 || p == nullptr) return NBODY_ERR_INVALID_ARG;
+    nbody_forces_opts o = {NBODY_PATH_AUTO, -1, 0, 0};
+    if (opts != nullptr) o = *opts;
+    if (o.path < NBODY_PATH_AUTO || o.path > NBODY_PATH_CLUSTER || o.splits < 0)
+        return NBODY_ERR_INVALID_ARG;
+    int path = o.path;
+    if (path == NBODY_PATH_AUTO) path = n <= kClusterMaxN ? NBODY_PATH_CLUSTER : NBODY_PATH_TILED;
+    if (path == NBODY_PATH_TILED) {
+        const int variant = o.variant < 0 ? kDefaultTiledVariant : o.variant;
+        if (variant >= nbody::tiled_variant_count()) return NBODY_ERR_INVALID_ARG;
+        plan_tiled(n, sm, tiled_occ[variant], variant, o.splits, p);
+        return NBODY_OK;
+    }
+    if (o.splits != 0) return NBODY_ERR_INVALID_ARG;   // the cluster path plans its own split
+    if (o.variant >= nbody::cluster_variant_count()) return NBODY_ERR_INVALID_ARG;
+    double best = INFINITY;
+    for (int v = 0; v < nbody::cluster_variant_count(); ++v) {
+        if (o.variant >= 0 && v != o.variant) continue;
+        nbody_plan cand;
+        double t;
+        plan_cluster_variant(n, sm, cluster_occ[v], v, &cand, &t);
+        if (t < best * (1.0 - 1e-3)) {
+            best = t;
+            *p = cand;
+        }
+    }
+    return NBODY_OK;
+}
+
+// Nominal occupancy of each tiled variant (used by the host-only planner
+// entry point when the caller gives none): register-limited at 64K per SM.
+int nominal_occ(int i_per_thread, int threads) {
+    const int regs = i_per_thread >= 8 ? 168 : (i_per_thread >= 4 ? 96 : 64);
+    int occ = 65536 / (regs * threads);
+    return occ < 1 ? 1 : occ;
+}
+
+}  // namespace
+
+// ======================================================================= C ABI
+
+extern "C" {
+
+const char *nbody_status_string(nbody_status s) {
+    switch (s) {
+        case NBODY_OK: return "NBODY_OK";
+        case NBODY_ERR_INVALID_ARG: return "NBODY_ERR_INVALID_ARG: invalid argument";
+        case NBODY_ERR_MISALIGNED: return "NBODY_ERR_MISALIGNED: body array not 16-byte aligned";
+        case NBODY_ERR_ALIAS: return "NBODY_ERR_ALIAS: output overlaps an input";
+        case NBODY_ERR_CUDA: return "NBODY_ERR_CUDA: CUDA runtime error";
+        case NBODY_ERR_TIMEOUT: return "NBODY_ERR_TIMEOUT: bounded device wait ran out";
+        case NBODY_ERR_DEVICE: return "NBODY_ERR_DEVICE: current device is not sm_103";
+    }
+    return "NBODY_ERR_UNKNOWN";
+}
+
+int nbody_last_cuda_error(void) { return g_last_cuda_error; }
+
+nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
+                               const nbody_forces_opts *opts, nbody_plan *plan) {
+    int occ[8], cocc[8];
+    for (int v = 0; v < nbody::tiled_variant_count() && v < 8; ++v) {
+        const nbody::TiledVariant &tv = nbody::tiled_variant(v);
+        occ[v] = ctas_per_sm > 0 ? ctas_per_sm : nominal_occ(tv.i_per_thread, tv.threads);
+    }
+    for (int v = 0; v < nbody::cluster_variant_count() && v < 8; ++v) {
+        const nbody::ClusterVariant &cv = nbody::cluster_variant(v);
+        cocc[v] = ctas_per_sm > 0 ? ctas_per_sm : nominal_occ(cv.i_per_thread, cv.warps * 32);
+    }
+    return make_plan(n, sm_count, occ, cocc, opts, plan);
+}
+
+nbody_status nbody_forces_ex(const float *pos_mass, int64_t n, float eps2, float *acc_pot,
+                             const nbody_forces_opts *opts, cudaStream_t stream) {
+    nbody_status st = check_forces(pos_mass, n, eps2, acc_pot);
+    if (st != NBODY_OK || n == 0) return st;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != NBODY_OK) return st;
+    nbody_plan plan;
+    if ((st = make_plan(n, dev->sm_count, dev->tiled_occ, dev->cluster_occ, opts, &plan)) != NBODY_OK)
+        return st;
+
+    const int ni = static_cast<int>(n);
+    float4 *out = reinterpret_cast<float4 *>(acc_pot);
+    const int ntiles = static_cast<int>(ceil_div(n, plan.tile));
+    cudaError_t e;
+    if (plan.path == NBODY_PATH_CLUSTER) {
+        e = nbody::launch_cluster(plan.variant, pos_mass, ni, eps2, plan.num_iblocks, plan.cluster,
+                                  plan.tiles_per_split, ntiles, out, stream);
+        return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
+    }
+    if (plan.splits == 1) {
+        e = nbody::launch_tiled(plan.variant, pos_mass, ni, eps2, plan.num_iblocks, 1,
+                                plan.tiles_per_split, ntiles, out, stream);
+        return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
+    }
+    void *scratch = nullptr;
+    e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.scratch_bytes), dev->pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    float4 *part = static_cast<float4 *>(scratch);
+    e = nbody::launch_tiled(plan.variant, pos_mass, ni, eps2, plan.num_iblocks, plan.splits,
+                            plan.tiles_per_split, ntiles, part, stream);
+    if (e == cudaSuccess)
+        e = nbody::launch_reduce_splits(part, ni, plan.splits, out, dev->sm_count, stream);
+    const cudaError_t ef = cudaFreeAsync(scratch, stream);
+    if (e == cudaSuccess) e = ef;
+    return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
+}
+
+nbody_status nbody_forces(const float *pos_mass, int64_t n, float eps2, float *acc_pot,
+                          cudaStream_t stream) {
+    return nbody_forces_ex(pos_mass, n, eps2, acc_pot, nullptr, stream);
+}
+
+nbody_status nbody_euler_step(float *pos_mass, float *vel, const float *acc_pot, int64_t n,
+                              float dt, cudaStream_t stream) {
+    if (check_n(n) != NBODY_OK) return NBODY_ERR_INVALID_ARG;
+    if (n == 0) return NBODY_OK;
+    if (pos_mass == nullptr || vel == nullptr || acc_pot == nullptr) return NBODY_ERR_INVALID_ARG;
+    if (!std::isfinite(dt)) return NBODY_ERR_INVALID_ARG;
+    if (!aligned16(pos_mass) || !aligned16(vel) || !aligned16(acc_pot)) return NBODY_ERR_MISALIGNED;
+    const int64_t bytes = 16 * n;
+    if (overlap(pos_mass, vel, bytes) || overlap(pos_mass, acc_pot, bytes) ||
+        overlap(vel, acc_pot, bytes))
+        return NBODY_ERR_ALIAS;
+    DeviceState *dev = nullptr;
+    nbody_status st = device_state(&dev);
+    if (st != NBODY_OK) return st;
+    const cudaError_t e = nbody::launch_euler(reinterpret_cast<float4 *>(pos_mass),
+                                              reinterpret_cast<float4 *>(vel),
+                                              reinterpret_cast<const float4 *>(acc_pot),
+                                              static_cast<int>(n), dt, dev->sm_count, stream);
+    return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// nbody_internal.h -- launchers behind the C ABI (not part of the public API).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nbody {
+
+// A compiled instantiation of the tiled force kernel.
+struct TiledVariant {
+    int i_per_thread;   // K target bodies per thread (even: lanes of f32x2 pairs)
+    int threads;        // threads per CTA
+    int tile;           // source bodies per shared-memory tile
+    const void *fn_pot; // kernel computing a and p
+};
+
+int tiled_variant_count();
+const TiledVariant &tiled_variant(int v);
+
+// Force kernel over grid = num_ib * splits CTAs; CTA b handles i-block
+// b % num_ib and source tiles [s * tps, min((s + 1) * tps, ntiles)) with
+// s = b / num_ib.  Writes out[s * n + i] (out = acc_pot when splits == 1).
+cudaError_t launch_tiled(int variant, const float *pos_mass, int n, float eps2, int num_ib,
+                         int splits, int tiles_per_split, int ntiles, float4 *out,
+                         cudaStream_t stream);
+
+// A compiled instantiation of the small-N cluster kernel.
+struct ClusterVariant {
+    int i_per_thread;   // K targets per lane (even); the cluster's target block is 32 K
+    int warps;          // W warps per CTA, each taking a slice of every source tile
+    int tile;           // source bodies per shared-memory tile
+    const void *fn_pot;
+};
+
+int cluster_variant_count();
+const ClusterVariant &cluster_variant(int v);
+
+// Cluster kernel over grid = num_ib * cluster CTAs in clusters of `cluster`;
+// cluster b handles targets [b * 32K, (b + 1) * 32K), its CTA of rank c the
+// source tiles [c * tpc, min((c + 1) * tpc, ntiles)).  Writes out[i] directly.
+cudaError_t launch_cluster(int variant, const float *pos_mass, int n, float eps2, int num_ib,
+                           int cluster, int tiles_per_cta, int ntiles, float4 *out,
+                           cudaStream_t stream);
+
+// out[i] = sum over s of part[s * n + i], in the order s = 0, 1, ..., compensated.
+cudaError_t launch_reduce_splits(const float4 *part, int n, int splits, float4 *out,
+                                 int sm_count, cudaStream_t stream);
+
+cudaError_t launch_euler(float4 *pos_mass, float4 *vel, const float4 *acc_pot, int n,
+                         float dt, int sm_count, cudaStream_t stream);
+
+}  // namespace nbody

@@ -1,0 +1,403 @@
+"""Benchmark: one step = nbody_forces (a + p) + nbody_euler_step on N = 2^20
+Plummer bodies (the headline workload), timed with CUDA events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config NAME] [--no-cpu-baseline] [--no-e2e]
+
+Prints one JSON line on rank 0.  `value` is interactions/s of the whole job
+(N^2 pairs per step and GPU) with inputs resident in HBM; `e2e` is the same
+metric through the C ABI with the step's inputs copied from pinned host
+memory and its results copied back inside the timed region.  L2 is flushed
+(a 256 MiB write) before every timed step, outside the step's events.
+
+--impl reference times the oracle (fp64 CPU, all host cores) on a bounded
+sample of the same workload: each step evaluates a fixed number of target
+rows against all N sources.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "interactions/s & GFLOP/s (20 flop/pair) at N=1M fp32, % of FP32/MUFU roofline"
+FLOPS_PER_PAIR = 20           # the pages' pair count (bodyBodyInteraction annotation)
+FP32_OPS_PER_PAIR = 13        # fp32 lane operations the pair law executes (a + p)
+FP32_LANES_PER_SM_CLK = 128
+RECIPE_SM_MAX_MHZ = 2070.0    # fallback if no measured peaks file is present
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="plummer1048576")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target seconds of oracle work for the CPU baseline sample")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "MEASURED_PEAKS.json"
+    return {}, "recipe fallback"
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def time_oracle(w, target_seconds, max_rows=None):
+    """Oracle interactions/s on a sample of target rows x all sources, sized to
+    about target_seconds of work after a short calibration."""
+    import oracle
+    n = w.n
+    probe = max(1, min(n, 8 * oracle.max_threads()))
+    oracle.forces(w.pos_mass, w.eps2, rows=range(min(n, oracle.max_threads())))   # wake the threads
+    t0 = time.perf_counter()
+    oracle.forces(w.pos_mass, w.eps2, rows=range(probe))
+    dt = max(time.perf_counter() - t0, 1e-6)
+    rows = int(max(probe, min(n, probe * target_seconds / dt)))
+    if max_rows:
+        rows = min(rows, max_rows)
+    t0 = time.perf_counter()
+    oracle.forces(w.pos_mass, w.eps2, rows=range(rows))
+    el = time.perf_counter() - t0
+    return {"value": rows * n / el, "unit": "interactions/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": el,
+            "sample": f"{rows} target rows x all {n} sources of {w.name} (fp64, OpenMP)",
+            "cpu_model": cpu_model()}
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons = [], [], set()
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def physical_gpu_index(local):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v.strip() for v in vis.split(",") if v.strip()]
+    if local < len(ids) and ids[local].isdigit():
+        return int(ids[local])
+    return local
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from all_pairs_gravitational_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    w = W.named(args.config)
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    # calibrate once, then every step evaluates the same row count
+    cal = time_oracle(w, per_step)
+    rows = int(cal["value"] * per_step / w.n) or 1
+    rows = min(rows, w.n)
+    for _ in range(args.warmup):
+        oracle.forces(w.pos_mass, w.eps2, rows=range(rows))
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.forces(w.pos_mass, w.eps2, rows=range(rows))
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = rows * w.n * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "interactions/s",
+        "gflops_20": value * FLOPS_PER_PAIR / 1e9, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "n": w.n, "eps2": float(w.eps2),
+                   "step": f"oracle forces for {rows} target rows x all {w.n} sources"},
+        "cpu_baseline": {"value": value, "unit": "interactions/s", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows} target rows x all {w.n} sources per step",
+                         "cpu_model": cpu_model()},
+        "e2e": {"value": value, "unit": "interactions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import all_pairs_gravitational_gb300 as apg
+    from all_pairs_gravitational_gb300 import workloads as W
+
+    world, rank, local = dist_setup(args)
+    device = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(device)
+    w = W.named(args.config)
+    n = w.n
+    pairs = float(n) * float(n)
+    plan = apg.nbody_plan_forces(n, props.multi_processor_count)
+    launches_per_step = (2 if plan["splits"] > 1 else 1) + 1
+
+    pm0 = torch.from_numpy(w.pos_mass).to(device)
+    vel0 = torch.from_numpy(w.vel).to(device)
+    pm = pm0.clone()
+    vel = vel0.clone()
+    acc = torch.empty_like(pm)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)   # 256 MiB > L2
+    stream = torch.cuda.current_stream(device)
+    eps2, dt = float(w.eps2), float(w.dt)
+
+    def step():
+        apg.nbody_forces(pm, eps2, acc)
+        apg.nbody_euler_step(pm, vel, acc, dt)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(physical_gpu_index(local))
+    barrier(world)
+    torch.cuda.synchronize()
+    with sampler:
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            apg.nbody_forces(pm, eps2, acc)
+            ev[k][1].record(stream)
+            apg.nbody_euler_step(pm, vel, acc, dt)
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    forces_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    euler_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms = sum(forces_ms + euler_ms) / args.steps
+    step_ms = max_over_ranks(step_ms, world)
+    clocks = sampler.summary()
+
+    peaks, peaks_src = measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz", RECIPE_SM_MAX_MHZ))
+    peak_pairs = props.multi_processor_count * sm_max * 1e6 * FP32_LANES_PER_SM_CLK / FP32_OPS_PER_PAIR
+    forces_s = statistics.mean(forces_ms) / 1e3
+    achieved = pairs / forces_s
+    euler_s = statistics.mean(euler_ms) / 1e3
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+
+    value = world * pairs / (step_ms / 1e3)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(apg, w, device, args.steps, world)
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        cpu = time_oracle(w, args.cpu_seconds)
+
+    sm_at_clock = clocks.get("sm_mhz")
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "interactions/s",
+        "gflops_20": value * FLOPS_PER_PAIR / 1e9,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "n": n, "eps2": eps2, "dt": dt,
+                   "step": "nbody_forces (a + p) then nbody_euler_step",
+                   "l2": "flushed (256 MiB write) before each timed step, outside its events",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "plan": {k: plan[k] for k in ("variant", "i_per_thread", "threads", "tile",
+                                                 "num_iblocks", "splits", "grid", "fill")}},
+        "roofline": {
+            "bound": "alu",
+            "achieved": achieved,
+            "peak": peak_pairs,
+            "unit": "interactions/s",
+            "frac": achieved / peak_pairs,
+            "traffic": None,
+            "kernel": "forces_tiled_kernel (+ split reduction)",
+            "peak_basis": (f"{props.multi_processor_count} SMs x {sm_max:.0f} MHz ({peaks_src}) x "
+                           f"{FP32_LANES_PER_SM_CLK} fp32 lanes / {FP32_OPS_PER_PAIR} fp32 ops per pair"),
+            "frac_at_sampled_clock": (achieved / (peak_pairs * sm_at_clock / sm_max)
+                                      if sm_at_clock else None),
+            "forces_ms": statistics.mean(forces_ms),
+            "gflops_20": achieved * FLOPS_PER_PAIR / 1e9,
+        },
+        "euler": {"ms": statistics.mean(euler_ms), "bytes": 80 * n,
+                  "gbs": 80 * n / euler_s / 1e9, "hbm_peak_gbs": hbm,
+                  "note": "inputs may be L2-resident at this size (84 MB < 129 MB L2)"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_loop": t_wall,
+        "device": props.name,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(apg, w, device, steps, world):
+    """Same metric through the C ABI from host buffers: per step, copy the
+    bodies and velocities in from pinned memory, compute, copy the new state
+    and the accelerations/potentials back."""
+    import torch
+    n = w.n
+    h_pm = torch.from_numpy(w.pos_mass).pin_memory()
+    h_vel = torch.from_numpy(w.vel).pin_memory()
+    h_out = [torch.empty((n, 4), dtype=torch.float32).pin_memory() for _ in range(3)]
+    d_pm = torch.empty((n, 4), device=device)
+    d_vel = torch.empty_like(d_pm)
+    d_acc = torch.empty_like(d_pm)
+    stream = torch.cuda.current_stream(device)
+    eps2, dt = float(w.eps2), float(w.dt)
+
+    def one():
+        d_pm.copy_(h_pm, non_blocking=True)
+        d_vel.copy_(h_vel, non_blocking=True)
+        apg.nbody_forces(d_pm, eps2, d_acc)
+        apg.nbody_euler_step(d_pm, d_vel, d_acc, dt)
+        h_out[0].copy_(d_pm, non_blocking=True)
+        h_out[1].copy_(d_vel, non_blocking=True)
+        h_out[2].copy_(d_acc, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    end.synchronize()
+    ms = start.elapsed_time(end) / steps
+    ms = max_over_ranks(ms, world)
+    return {"value": world * float(n) * n / (ms / 1e3), "unit": "interactions/s",
+            "h2d_bytes_per_step": 32 * n, "d2h_bytes_per_step": 48 * n, "ms_per_step": ms}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+"""Host-side checks of the C ABI: no GPU and no compute call needed.
+
+The library loads, exports every function include/nbody.h declares, rejects
+bad arguments before touching CUDA, and plans launches that cover every
+target and source exactly once.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import all_pairs_gravitational_gb300 as apg
+from all_pairs_gravitational_gb300 import _binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "nbody.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return apg.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nbody_\w+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert _declared_functions() == sorted(apg.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in _binding.STATUS_NAMES.items():
+        assert apg.nbody_status_string(code).startswith(name)
+    assert "UNKNOWN" in apg.nbody_status_string(99)
+
+
+P = 1 << 20          # a fake, 16-byte aligned "device" address: never dereferenced
+
+
+def _forces(lib, pm, n, eps2, acc):
+    return lib.nbody_forces(ctypes.c_void_p(pm), n, ctypes.c_float(eps2), ctypes.c_void_p(acc),
+                            None)
+
+
+def test_forces_argument_checks(lib):
+    # nothing below reaches CUDA: each call is rejected (or is a no-op) on the host
+    assert _forces(lib, P, 0, 1e-4, P + 4096) == 0                   # n == 0: no-op
+    assert _forces(lib, 0, 0, 1e-4, 0) == 0
+    assert _forces(lib, P, -1, 1e-4, P + 4096) == 1
+    assert _forces(lib, P, 2 ** 31, 1e-4, P + 2 ** 36) == 1
+    assert _forces(lib, 0, 10, 1e-4, P) == 1                         # null input
+    assert _forces(lib, P, 10, 1e-4, 0) == 1                         # null output
+    for bad in (0.0, -1e-4, float("nan"), float("inf"), 1e-40):      # 1e-40 is subnormal
+        assert _forces(lib, P, 10, bad, P + 4096) == 1, bad
+    assert _forces(lib, P + 4, 10, 1e-4, P + 4096) == 2              # misaligned input
+    assert _forces(lib, P, 10, 1e-4, P + 4104) == 2                  # misaligned output
+    assert _forces(lib, P, 10, 1e-4, P) == 3                         # same buffer
+    assert _forces(lib, P, 10, 1e-4, P + 144) == 3                   # overlaps the last body
+    assert _forces(lib, P + 144, 10, 1e-4, P) == 3
+
+
+def test_euler_argument_checks(lib):
+    def call(pm, v, a, n, dt):
+        return lib.nbody_euler_step(ctypes.c_void_p(pm), ctypes.c_void_p(v), ctypes.c_void_p(a), n,
+                                    ctypes.c_float(dt), None)
+    a, b, c = P, P + 4096, P + 8192
+    assert call(a, b, c, 0, 1e-3) == 0
+    assert call(a, b, c, -5, 1e-3) == 1
+    assert call(0, b, c, 5, 1e-3) == 1
+    assert call(a, b, c, 5, float("nan")) == 1
+    assert call(a, b, c, 5, float("inf")) == 1
+    assert call(a + 8, b, c, 5, 1e-3) == 2
+    assert call(a, b, c + 8, 5, 1e-3) == 2
+    assert call(a, a + 64, c, 5, 1e-3) == 3       # pos and vel overlap
+    assert call(a, b, b + 16, 5, 1e-3) == 3       # vel and acc overlap
+    assert call(a, b, a, 5, 1e-3) == 3            # acc is pos
+
+
+def _covers(plan, n):
+    """Every target in exactly one target block, every source tile in exactly
+    one piece of the source range."""
+    ntiles = -(-n // plan["tile"])
+    if plan["path"] == apg.NBODY_PATH_TILED:
+        bi = plan["threads"] * plan["i_per_thread"]
+        tps, s = plan["tiles_per_split"], plan["splits"]
+        assert plan["grid"] == plan["num_iblocks"] * s
+        assert plan["scratch_bytes"] == (16 * s * n if s > 1 else 0)
+    else:
+        assert plan["path"] == apg.NBODY_PATH_CLUSTER
+        bi = 32 * plan["i_per_thread"]
+        tps, s = plan["tiles_per_split"], plan["cluster"]
+        assert s in (1, 2, 4, 8)
+        assert plan["splits"] == s * plan["warps_j"]
+        assert plan["threads"] == 32 * plan["warps_j"]
+        assert plan["tile"] % plan["warps_j"] == 0 and plan["tile"] // plan["warps_j"] <= 32
+        assert plan["grid"] == plan["num_iblocks"] * s
+        assert plan["scratch_bytes"] == 0
+    assert plan["num_iblocks"] * bi >= n > (plan["num_iblocks"] - 1) * bi
+    assert s * tps >= ntiles > (s - 1) * tps
+    assert plan["grid"] < 2 ** 31
+    assert 0 < plan["fill"] <= 1.0
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 31, 33, 127, 128, 129, 255, 257, 1000, 1024, 4096,
+                               16384, 65536, 200003, 1048576, 2 ** 24 + 3, 2 ** 31 - 1])
+@pytest.mark.parametrize("sm", [1, 148, 152, 160])
+def test_plan_covers_all_pairs(lib, n, sm):
+    plan = apg.nbody_plan_forces(n, sm)
+    _covers(plan, n)
+
+
+def test_plan_fills_the_gpu_at_one_million():
+    plan = apg.nbody_plan_forces(1048576, 152)
+    assert plan["fill"] > 0.97
+    one = apg.nbody_plan_forces(1048576, 152, splits=1)
+    assert one["splits"] == 1 and one["scratch_bytes"] == 0
+    assert plan["fill"] > one["fill"]
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 33, 127, 129, 1000, 1024, 2048, 4096, 8192, 12288, 16384])
+@pytest.mark.parametrize("variant", [-1, 0, 1, 2, 3])
+def test_cluster_plan_covers_all_pairs(n, variant):
+    plan = apg.nbody_plan_forces(n, 152, path=apg.NBODY_PATH_CLUSTER, variant=variant)
+    _covers(plan, n)
+    if variant >= 0:
+        assert plan["variant"] == variant
+
+
+def test_auto_path_choice():
+    assert apg.nbody_plan_forces(1024, 152)["path"] == apg.NBODY_PATH_CLUSTER
+    assert apg.nbody_plan_forces(8192, 152)["path"] == apg.NBODY_PATH_CLUSTER
+    assert apg.nbody_plan_forces(1048576, 152)["path"] == apg.NBODY_PATH_TILED
+    with pytest.raises(apg.NbodyError):
+        apg.nbody_plan_forces(1000, 152, path=apg.NBODY_PATH_CLUSTER, splits=3)
+    with pytest.raises(apg.NbodyError):
+        apg.nbody_plan_forces(1000, 152, path=7)
+
+
+def test_plan_forced_splits_and_variants(lib):
+    for v in range(4):
+        for s in (1, 2, 7, 64):
+            plan = apg.nbody_plan_forces(200003, 152, path=apg.NBODY_PATH_TILED, variant=v,
+                                         splits=s)
+            _covers(plan, 200003)
+            assert plan["variant"] == v
+    with pytest.raises(apg.NbodyError):
+        apg.nbody_plan_forces(1000, 152, variant=99)
+    with pytest.raises(apg.NbodyError):
+        apg.nbody_plan_forces(0, 152)
+    with pytest.raises(apg.NbodyError):
+        apg.nbody_plan_forces(1000, 0)

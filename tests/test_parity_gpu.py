@@ -1,0 +1,284 @@
+"""Parity of the CUDA path with the oracle, through the C ABI (needs a GPU).
+
+Tolerances: relative L2 error of the accelerations (all 3N components) and
+of the potentials <= 1e-5; largest per-body relative error <= 1e-4 for |a|
+and for |p|; the Euler step bit-identical given the same accelerations.
+"""
+import numpy as np
+import pytest
+import torch
+
+import all_pairs_gravitational_gb300 as apg
+import oracle
+from all_pairs_gravitational_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+L2_TOL = 1e-5
+BODY_TOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "these tests need a CUDA GPU"
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def _rel(diff, scale):
+    """diff / scale, where a zero reference must be matched exactly."""
+    diff = np.asarray(diff, np.float64)
+    scale = np.asarray(scale, np.float64)
+    exact = np.where(diff == 0, 0.0, np.inf)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return np.where(scale > 0, diff / np.where(scale > 0, scale, 1.0), exact)
+
+
+def errors(got, ref, rows=None, potential=True):
+    got = np.asarray(got, np.float64)
+    if rows is not None:
+        got = got[rows]
+    ea = float(_rel(np.linalg.norm(got[:, :3] - ref[:, :3]), np.linalg.norm(ref[:, :3])))
+    na = np.linalg.norm(ref[:, :3], axis=1)
+    ba = float(_rel(np.linalg.norm(got[:, :3] - ref[:, :3], axis=1), na).max())
+    out = {"l2_a": ea, "body_a": ba}
+    if potential:
+        out["l2_p"] = np.linalg.norm(got[:, 3] - ref[:, 3]) / np.linalg.norm(ref[:, 3])
+        out["body_p"] = (np.abs(got[:, 3] - ref[:, 3]) / np.abs(ref[:, 3])).max()
+    return out
+
+
+def assert_parity(got, ref, rows=None, potential=True):
+    e = errors(got, ref, rows, potential)
+    assert e["l2_a"] <= L2_TOL and e["body_a"] <= BODY_TOL, e
+    if potential:
+        assert e["l2_p"] <= L2_TOL and e["body_p"] <= BODY_TOL, e
+    return e
+
+
+def gpu_forces(pm_np, eps2, **kw):
+    pm = torch.from_numpy(np.ascontiguousarray(pm_np)).to(dev())
+    acc = apg.nbody_forces_ex(pm, float(eps2), **kw)
+    torch.cuda.synchronize()
+    return acc.cpu().numpy()
+
+
+def sample_rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    rows = rng.choice(n, size=min(k, n), replace=False)
+    return np.unique(np.concatenate([rows, [0, n - 1]]))
+
+
+# ------------------------------------------------------------ configurations
+
+def test_disk4096_acceleration_and_euler():
+    w = W.named("disk4096")
+    acc = gpu_forces(w.pos_mass, w.eps2)
+    ref = oracle.forces(w.pos_mass, w.eps2)
+    assert_parity(acc, ref, potential=False)
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    vel = torch.from_numpy(w.vel).to(dev())
+    a = torch.from_numpy(acc).to(dev())
+    apg.nbody_euler_step(pm, vel, a, float(w.dt))
+    torch.cuda.synchronize()
+    pm_ref, v_ref = oracle.euler(w.pos_mass, w.vel, acc, w.dt)
+    assert np.array_equal(pm.cpu().numpy(), pm_ref)
+    assert np.array_equal(vel.cpu().numpy(), v_ref)
+
+
+def test_cube16384_full():
+    w = W.named("cube16384")
+    assert_parity(gpu_forces(w.pos_mass, w.eps2), oracle.forces(w.pos_mass, w.eps2))
+
+
+def test_plummer65536_ten_steps():
+    """Ten force + Euler steps on the GPU's own state; parity on sampled rows
+    at every step and the Euler step bit-exact every step."""
+    w = W.named("plummer65536")
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    vel = torch.from_numpy(w.vel).to(dev())
+    acc = torch.empty_like(pm)
+    for step in range(w.steps):
+        apg.nbody_forces(pm, float(w.eps2), acc)
+        torch.cuda.synchronize()
+        pm_np, v_np, a_np = pm.cpu().numpy(), vel.cpu().numpy(), acc.cpu().numpy()
+        rows = sample_rows(w.n, 1024, step)
+        ref = oracle.forces(pm_np, w.eps2, rows=rows)
+        assert_parity(a_np, ref, rows)
+        apg.nbody_euler_step(pm, vel, acc, float(w.dt))
+        torch.cuda.synchronize()
+        pm_ref, v_ref = oracle.euler(pm_np, v_np, a_np, w.dt)
+        assert np.array_equal(pm.cpu().numpy(), pm_ref), step
+        assert np.array_equal(vel.cpu().numpy(), v_ref), step
+
+
+def test_clumps200003_sampled():
+    w = W.named("clumps200003")
+    acc = gpu_forces(w.pos_mass, w.eps2)
+    rows = sample_rows(w.n, 2048, 1)
+    # include the ragged last tile and the last i-block
+    rows = np.unique(np.concatenate([rows, np.arange(w.n - 300, w.n)]))
+    assert_parity(acc, oracle.forces(w.pos_mass, w.eps2, rows=rows), rows)
+
+
+@pytest.mark.slow
+def test_plummer1048576_sampled_in_bench_configuration():
+    """The full-size workload in the launch configuration the benchmark times
+    (default plan), checked on sampled rows."""
+    w = W.named("plummer1048576")
+    acc = gpu_forces(w.pos_mass, w.eps2)
+    rows = sample_rows(w.n, 768, 2)
+    assert_parity(acc, oracle.forces(w.pos_mass, w.eps2, rows=rows), rows)
+    plan = apg.nbody_plan_forces(w.n, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["splits"] >= 1
+
+
+@pytest.mark.parametrize("n", W.SMALL_SWEEP)
+def test_small_cube_sweep(n):
+    w = W.small_cube(n)
+    assert_parity(gpu_forces(w.pos_mass, w.eps2), oracle.forces(w.pos_mass, w.eps2))
+
+
+# ------------------------------------------------------------ edges and plans
+
+@pytest.mark.parametrize("n", [1, 2, 3, 31, 33, 127, 129, 255, 257, 511, 513, 1000, 1025, 4097])
+def test_ragged_sizes(n):
+    w = W.cube(n, seed=n + 17)
+    assert_parity(gpu_forces(w.pos_mass, w.eps2), oracle.forces(w.pos_mass, w.eps2))
+
+
+def test_single_body_self_term():
+    pm = np.array([[0.25, -1.5, 3.0, 2.0]], np.float32)
+    out = gpu_forces(pm, 0.0625)
+    assert out[0, :3].tolist() == [0.0, 0.0, 0.0]
+    assert out[0, 3] == pytest.approx(-8.0, rel=1e-6)
+
+
+def test_two_body_closed_form():
+    pm = np.array([[0, 0, 0, 1], [4, 0, 0, 2]], np.float32)
+    out = gpu_forces(pm, 9.0).astype(np.float64)
+    np.testing.assert_allclose(out[:, 0], [8 / 125, -4 / 125], rtol=1e-6)
+    np.testing.assert_allclose(out[:, 3], [-11 / 15, -13 / 15], rtol=1e-6)
+    assert np.all(out[:, 1:3] == 0)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 40])
+def test_forced_plans(variant, splits):
+    w = W.clumps(5003, seed=77)
+    ref = oracle.forces(w.pos_mass, w.eps2)
+    got = gpu_forces(w.pos_mass, w.eps2, path=apg.NBODY_PATH_TILED, variant=variant,
+                     splits=splits)
+    assert_parity(got, ref)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_disk_near_neighbours_both_paths(path):
+    """The disk workload has bodies whose nearest neighbours contribute terms
+    hundreds of times |a_i| (condition number ~1e3): the per-body bound holds."""
+    w = W.named("disk4096")
+    got = gpu_forces(w.pos_mass, w.eps2, path=path)
+    assert_parity(got, oracle.forces(w.pos_mass, w.eps2), potential=False)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("n", [1, 3, 100, 1000, 4096, 5003, 12000])
+def test_cluster_path(variant, n):
+    w = W.cube(n, seed=n + 3)
+    got = gpu_forces(w.pos_mass, w.eps2, path=apg.NBODY_PATH_CLUSTER, variant=variant)
+    assert_parity(got, oracle.forces(w.pos_mass, w.eps2))
+
+
+def test_paths_agree_small_n():
+    """Both paths on the same input: each within tolerance of the oracle."""
+    w = W.small_cube(2048)
+    ref = oracle.forces(w.pos_mass, w.eps2)
+    for path in (apg.NBODY_PATH_TILED, apg.NBODY_PATH_CLUSTER):
+        assert_parity(gpu_forces(w.pos_mass, w.eps2, path=path), ref)
+
+
+def test_cluster_path_deterministic():
+    w = W.small_cube(4096)
+    a = gpu_forces(w.pos_mass, w.eps2, path=apg.NBODY_PATH_CLUSTER)
+    for _ in range(3):
+        assert np.array_equal(gpu_forces(w.pos_mass, w.eps2, path=apg.NBODY_PATH_CLUSTER), a)
+
+
+def test_bitwise_deterministic():
+    w = W.clumps(30011, seed=5)
+    a = gpu_forces(w.pos_mass, w.eps2)
+    for _ in range(3):
+        assert np.array_equal(gpu_forces(w.pos_mass, w.eps2), a)
+
+
+def test_newtons_third_law_on_gpu():
+    w = W.clumps(20000, seed=8)
+    acc = gpu_forces(w.pos_mass, w.eps2).astype(np.float64)
+    m = w.pos_mass[:, 3].astype(np.float64)[:, None]
+    total = np.abs((m * acc[:, :3]).sum(0)).max()
+    assert total < 1e-6 * (m * np.abs(acc[:, :3])).sum()
+
+
+def test_canaries_and_offsets_untouched():
+    """Output written exactly in [0, n): records before and after are intact."""
+    w = W.cube(3001, seed=3)
+    n = w.n
+    big = torch.full((n + 8, 4), 12345.0, device=dev())
+    out = big[4:4 + n]
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    apg.nbody_forces(pm, float(w.eps2), out)
+    torch.cuda.synchronize()
+    b = big.cpu().numpy()
+    assert np.all(b[:4] == 12345.0) and np.all(b[-4:] == 12345.0)
+    assert_parity(b[4:4 + n], oracle.forces(w.pos_mass, w.eps2))
+    assert np.array_equal(pm.cpu().numpy(), w.pos_mass)          # input untouched
+
+
+def test_side_stream():
+    w = W.cube(2000, seed=4)
+    s = torch.cuda.Stream()
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    with torch.cuda.stream(s):
+        acc = apg.nbody_forces(pm, float(w.eps2))
+    s.synchronize()
+    assert_parity(acc.cpu().numpy(), oracle.forces(w.pos_mass, w.eps2))
+
+
+def test_empty_input_is_a_noop():
+    pm = torch.empty((0, 4), device=dev())
+    acc = apg.nbody_forces(pm, 1e-4)
+    assert acc.shape == (0, 4)
+    apg.nbody_euler_step(pm, torch.empty_like(pm), acc, 1e-3)
+
+
+def test_host_rejections_on_gpu_tensors():
+    pm = torch.zeros((17, 4), device=dev())
+    flat = torch.zeros(17 * 4 + 1, device=dev())
+    mis = flat[1:].view(17, 4)                                    # 4 bytes off alignment
+    with pytest.raises(apg.NbodyError) as e:
+        apg.nbody_forces(mis, 1e-4)
+    assert e.value.status == 2
+    with pytest.raises(apg.NbodyError) as e:
+        apg.nbody_forces(pm, 1e-4, pm)
+    assert e.value.status == 3
+    with pytest.raises(apg.NbodyError) as e:
+        apg.nbody_forces(pm, 0.0)
+    assert e.value.status == 1
+
+
+def test_euler_large_bit_exact():
+    w = W.plummer(300007, seed=1)
+    acc = np.zeros_like(w.pos_mass)
+    acc[:, :3] = W.Stream(9).uniform(3 * w.n, -50, 50).reshape(w.n, 3)
+    acc[:, 3] = 7.0
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    vel = torch.from_numpy(w.vel).to(dev())
+    apg.nbody_euler_step(pm, vel, torch.from_numpy(acc).to(dev()), float(w.dt))
+    torch.cuda.synchronize()
+    pm_ref, v_ref = oracle.euler(w.pos_mass, w.vel, acc, w.dt)
+    assert np.array_equal(pm.cpu().numpy(), pm_ref)
+    assert np.array_equal(vel.cpu().numpy(), v_ref)
