@@ -20,12 +20,14 @@ NBODY_PATH_CLUSTER = 2
 
 STATUS_NAMES = {
     0: "NBODY_OK", 1: "NBODY_ERR_INVALID_ARG", 2: "NBODY_ERR_MISALIGNED", 3: "NBODY_ERR_ALIAS",
-    4: "NBODY_ERR_CUDA", 5: "NBODY_ERR_TIMEOUT", 6: "NBODY_ERR_DEVICE",
+    4: "NBODY_ERR_CUDA", 5: "NBODY_ERR_TIMEOUT", 6: "NBODY_ERR_DEVICE", 7: "NBODY_ERR_TOO_LARGE",
 }
+
+NBODY_NOALLOC_MAX_N = 4194304
 
 # Every symbol include/nbody.h declares (checked by the tests).
 EXPORTS = ["nbody_forces", "nbody_euler_step", "nbody_status_string", "nbody_last_cuda_error",
-           "nbody_plan_forces", "nbody_forces_ex"]
+           "nbody_plan_forces", "nbody_forces_ex", "nbody_forces_noalloc"]
 
 
 class nbody_forces_opts(ctypes.Structure):
@@ -66,6 +68,7 @@ _SIGS = {
     "nbody_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "nbody_last_cuda_error": ([], ctypes.c_int),
     "nbody_plan_forces": ([ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P], ctypes.c_int),
+    "nbody_forces_noalloc": ([_P, ctypes.c_int64, ctypes.c_float, _P, _P], ctypes.c_int),
 }
 
 
@@ -146,6 +149,24 @@ def nbody_forces_ex(pos_mass, eps2, acc_pot=None, path=NBODY_PATH_AUTO, variant=
                                  ctypes.byref(opts), _stream_handle(pos_mass.device, stream))
     if st != 0:
         raise NbodyError(st, "nbody_forces")
+    return acc_pot
+
+
+def nbody_forces_noalloc(pos_mass, eps2, acc_pot, stream=None):
+    """nbody_forces computed with the library's fixed scratch: the C call
+    allocates nothing, so acc_pot must be given (n <= NBODY_NOALLOC_MAX_N)."""
+    import torch
+    lib = load_library()
+    _bodies(pos_mass, "pos_mass")
+    n = pos_mass.shape[0]
+    _bodies(acc_pot, "acc_pot", n)
+    if acc_pot.device != pos_mass.device:
+        raise ValueError("pos_mass and acc_pot must be on the same device")
+    with torch.cuda.device(pos_mass.device):
+        st = lib.nbody_forces_noalloc(_ptr(pos_mass), n, ctypes.c_float(float(eps2)),
+                                      _ptr(acc_pot), _stream_handle(pos_mass.device, stream))
+    if st != 0:
+        raise NbodyError(st, "nbody_forces_noalloc")
     return acc_pot
 
 

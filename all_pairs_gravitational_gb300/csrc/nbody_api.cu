@@ -263,6 +263,8 @@ const char *nbody_status_string(nbody_status s) {
         case NBODY_ERR_CUDA: return "NBODY_ERR_CUDA: CUDA runtime error";
         case NBODY_ERR_TIMEOUT: return "NBODY_ERR_TIMEOUT: bounded device wait ran out";
         case NBODY_ERR_DEVICE: return "NBODY_ERR_DEVICE: current device is not sm_103";
+        case NBODY_ERR_TOO_LARGE:
+            return "NBODY_ERR_TOO_LARGE: n exceeds the fixed scratch of nbody_forces_noalloc";
     }
     return "NBODY_ERR_UNKNOWN";
 }

@@ -46,7 +46,8 @@ typedef enum nbody_status {
     NBODY_ERR_ALIAS = 3,        /* an output overlaps an input it must not overlap */
     NBODY_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed (see nbody_last_cuda_error) */
     NBODY_ERR_TIMEOUT = 5,      /* reserved: a bounded device-side wait ran out */
-    NBODY_ERR_DEVICE = 6        /* the current device is not an sm_103 GPU */
+    NBODY_ERR_DEVICE = 6,       /* the current device is not an sm_103 GPU */
+    NBODY_ERR_TOO_LARGE = 7     /* n above NBODY_NOALLOC_MAX_N (nbody_forces_noalloc only) */
 } nbody_status;
 
 /*
@@ -142,6 +143,39 @@ nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
 /* nbody_forces with explicit launch options (NULL = defaults). */
 nbody_status nbody_forces_ex(const float *pos_mass, int64_t n, float eps2, float *acc_pot,
                              const nbody_forces_opts *opts, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * No-allocation variant.  The pages have no counterpart to this call: it
+ * exists for callers that cannot allocate device memory -- a host framework
+ * that owns all GPU memory and forbids libraries from allocating, code under
+ * a hard latency budget (cudaMalloc/cudaFree can synchronise the device), or
+ * code whose memory budget is fixed up front.
+ * ------------------------------------------------------------------------ */
+
+/* Largest n nbody_forces_noalloc accepts: its fixed scratch holds this many
+ * float4 partial records (64 MiB), and it splits the source range into S
+ * pieces only while S * n fits. */
+#define NBODY_NOALLOC_MAX_N 4194304
+
+/*
+ * nbody_forces_noalloc -- the same operation, arguments and result layout as
+ * nbody_forces, computed by the tiled path with its split partials in a
+ * fixed array inside the library instead of memory obtained per call.  It
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   - Every GPU that loads libnbody.so holds that array (64 MiB) until the
+ *     process exits.
+ *   - The first call on a device does a one-time set-up for it (device
+ *     attributes, occupancy, and the array's device address); make that first
+ *     call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls whose kernels overlap on
+ *     the GPU (other streams, other host threads) race on it: serialise them.
+ *   - n > NBODY_NOALLOC_MAX_N returns NBODY_ERR_TOO_LARGE and launches
+ *     nothing; the other errors are those of nbody_forces.
+ */
+nbody_status nbody_forces_noalloc(const float *pos_mass, int64_t n, float eps2,
+                                  float *acc_pot, cudaStream_t stream);
 
 #ifdef __cplusplus
 }
