@@ -69,8 +69,51 @@ __device__ __forceinline__ void stage_tile(float *sbuf, const float *pm, int n, 
     }
 }
 
-template <int K, int NT, int P, bool POT>
-__global__ void __launch_bounds__(NT)
+// Compensated totals of one thread: in registers, or (TSMEM) in shared
+// memory, one column per thread so that a warp's accesses are contiguous.
+// Shared-memory totals free 8 registers per target pair for occupancy at
+// the cost of 4 shared accesses per component per fold.
+template <int KP, int NT, bool TSMEM>
+struct Totals;
+
+template <int KP, int NT>
+struct Totals<KP, NT, false> {
+    f2 h[KP][4], l[KP][4];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int q = 0; q < KP; ++q)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) h[q][c] = l[q][c] = 0ull;
+    }
+    __device__ __forceinline__ void fold(int q, int c, f2 &part) { f2_kahan_fold(h[q][c], l[q][c], part); }
+    __device__ __forceinline__ f2 value(int q, int c) { return f2_sub(h[q][c], l[q][c]); }
+};
+
+template <int KP, int NT>
+struct Totals<KP, NT, true> {
+    f2 (*s)[NT];     // [KP * 4 * 2][NT]: (hi, lo) of component c of pair q
+    int tid;
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int r = 0; r < KP * 8; ++r) s[r][tid] = 0ull;
+    }
+    __device__ __forceinline__ void fold(int q, int c, f2 &part) {
+        f2 hi = s[(q * 4 + c) * 2][tid];
+        f2 lo = s[(q * 4 + c) * 2 + 1][tid];
+        f2_kahan_fold(hi, lo, part);
+        s[(q * 4 + c) * 2][tid] = hi;
+        s[(q * 4 + c) * 2 + 1][tid] = lo;
+    }
+    __device__ __forceinline__ f2 value(int q, int c) {
+        return f2_sub(s[(q * 4 + c) * 2][tid], s[(q * 4 + c) * 2 + 1][tid]);
+    }
+};
+
+// MODE 0: one source per step of the unrolled loop; 1: software-pipelined
+// (rsqrt of source j+1 issued before source j is finished); 2: two sources
+// per step, their instructions interleaved in source order.
+template <int K, int NT, int P, int MINB, bool TSMEM, int U, int MODE, bool POT>
+__global__ void __launch_bounds__(NT, MINB)
 forces_tiled_kernel(const float *__restrict__ pm, int n, float eps2, int num_ib,
                     int tiles_per_split, int ntiles, float4 *__restrict__ out) {
     static_assert(K % 2 == 0, "targets are processed in f32x2 pairs");
@@ -78,7 +121,11 @@ forces_tiled_kernel(const float *__restrict__ pm, int n, float eps2, int num_ib,
     constexpr int FOLD_P = (1024 + P - 1) / P;   // tiles between folds of the potential
     static_assert(P % kFoldJ == 0, "tile must hold whole fold intervals");
 
-    __shared__ __align__(16) float sdup[kStages][P * 8];
+    // One spare body per stage: the software-pipelined loop reads source
+    // jj + 1 ahead of finishing jj, and the last look-ahead lands on the spare
+    // slot; its values are never used.
+    __shared__ __align__(16) float sdup[kStages][(P + 1) * 8];
+    __shared__ __align__(16) f2 stot[TSMEM ? KP * 8 : 1][TSMEM ? NT : 1];
 
     const int tid = static_cast<int>(threadIdx.x);
     const int ib = static_cast<int>(blockIdx.x % static_cast<unsigned>(num_ib));
@@ -102,15 +149,15 @@ forces_tiled_kernel(const float *__restrict__ pm, int n, float eps2, int num_ib,
     }
     const f2 e2 = f2_pack(eps2, eps2);
 
-    f2 ax[KP], ay[KP], az[KP], pp[KP];          // fp32 partial over the current fold
-    f2 hx[KP], hy[KP], hz[KP], hp[KP];          // compensated totals: hi ...
-    f2 lx[KP], ly[KP], lz[KP], lp[KP];          // ... and the Kahan correction
+    f2 ax[KP], ay[KP], az[KP], pp[KP];          // fp32 partials of the current fold
 #pragma unroll
-    for (int q = 0; q < KP; ++q) {
-        ax[q] = ay[q] = az[q] = pp[q] = 0ull;
-        hx[q] = hy[q] = hz[q] = hp[q] = 0ull;
-        lx[q] = ly[q] = lz[q] = lp[q] = 0ull;
+    for (int q = 0; q < KP; ++q) ax[q] = ay[q] = az[q] = pp[q] = 0ull;
+    Totals<KP, NT, TSMEM> tot;
+    if constexpr (TSMEM) {
+        tot.s = stot;
+        tot.tid = tid;
     }
+    tot.init();
 
     // Prologue: two tiles in flight (one commit group per tile, empty past the end).
     if (t_begin < t_end) stage_tile<NT, P>(sdup[0], pm, n, t_begin);
@@ -131,9 +178,108 @@ forces_tiled_kernel(const float *__restrict__ pm, int n, float eps2, int num_ib,
         }
 
         const float4 *s4 = reinterpret_cast<const float4 *>(sdup[stage]);
+        if constexpr (MODE == 1) {
+            // front(j): r = x_j - x_i, d2, rsqrt(d2) -- issued one source
+            // ahead, so the MUFU work of j+1 overlaps the FMA work of j.
+            f2 cdx[KP], cdy[KP], cdz[KP], cinv[KP], cm;
+            auto front = [&](int j, f2 (&dx)[KP], f2 (&dy)[KP], f2 (&dz)[KP], f2 (&inv)[KP], f2 &m) {
+                const float4 a = s4[2 * j];
+                const float4 b = s4[2 * j + 1];
+                const f2 xj = f2_pack(a.x, a.y);
+                const f2 yj = f2_pack(a.z, a.w);
+                const f2 zj = f2_pack(b.x, b.y);
+                m = f2_pack(b.z, b.w);
+#pragma unroll
+                for (int q = 0; q < KP; ++q) {
+                    dx[q] = f2_sub(xj, xi[q]);
+                    dy[q] = f2_sub(yj, yi[q]);
+                    dz[q] = f2_sub(zj, zi[q]);
+                    f2 d2 = f2_fma(dx[q], dx[q], e2);
+                    d2 = f2_fma(dy[q], dy[q], d2);
+                    d2 = f2_fma(dz[q], dz[q], d2);
+                    float d2a, d2b;
+                    f2_unpack(d2, d2a, d2b);
+                    inv[q] = f2_pack(rsqrt_hw(d2a), rsqrt_hw(d2b));
+                }
+            };
+            front(0, cdx, cdy, cdz, cinv, cm);
+#pragma unroll U
+            for (int jj = 0; jj < P; ++jj) {
+                f2 ndx[KP], ndy[KP], ndz[KP], ninv[KP], nm;
+                front(jj + 1, ndx, ndy, ndz, ninv, nm);     // jj + 1 == P: the spare slot
+#pragma unroll
+                for (int q = 0; q < KP; ++q) {
+                    const f2 tm = f2_mul(cm, cinv[q]);
+                    const f2 inv2 = f2_mul(cinv[q], cinv[q]);
+                    const f2 sc = f2_mul(tm, inv2);
+                    ax[q] = f2_fma(sc, cdx[q], ax[q]);
+                    ay[q] = f2_fma(sc, cdy[q], ay[q]);
+                    az[q] = f2_fma(sc, cdz[q], az[q]);
+                    if (POT) pp[q] = f2_add(pp[q], tm);
+                    cdx[q] = ndx[q];
+                    cdy[q] = ndy[q];
+                    cdz[q] = ndz[q];
+                    cinv[q] = ninv[q];
+                }
+                cm = nm;
+                if ((jj % kFoldJ) == kFoldJ - 1) {
+#pragma unroll
+                    for (int q = 0; q < KP; ++q) {
+                        tot.fold(q, 0, ax[q]);
+                        tot.fold(q, 1, ay[q]);
+                        tot.fold(q, 2, az[q]);
+                    }
+                }
+            }
+        } else if constexpr (MODE == 2) {
+#pragma unroll 1
+            for (int jb = 0; jb < P; jb += kFoldJ) {
+#pragma unroll U
+                for (int jj = jb; jj < jb + kFoldJ; jj += 2) {
+                    const float4 a0 = s4[2 * jj], b0 = s4[2 * jj + 1];
+                    const float4 a1 = s4[2 * jj + 2], b1 = s4[2 * jj + 3];
+                    const f2 xj0 = f2_pack(a0.x, a0.y), xj1 = f2_pack(a1.x, a1.y);
+                    const f2 yj0 = f2_pack(a0.z, a0.w), yj1 = f2_pack(a1.z, a1.w);
+                    const f2 zj0 = f2_pack(b0.x, b0.y), zj1 = f2_pack(b1.x, b1.y);
+                    const f2 mj0 = f2_pack(b0.z, b0.w), mj1 = f2_pack(b1.z, b1.w);
+#pragma unroll
+                    for (int q = 0; q < KP; ++q) {
+                        const f2 dx0 = f2_sub(xj0, xi[q]), dx1 = f2_sub(xj1, xi[q]);
+                        const f2 dy0 = f2_sub(yj0, yi[q]), dy1 = f2_sub(yj1, yi[q]);
+                        const f2 dz0 = f2_sub(zj0, zi[q]), dz1 = f2_sub(zj1, zi[q]);
+                        f2 d20 = f2_fma(dx0, dx0, e2), d21 = f2_fma(dx1, dx1, e2);
+                        d20 = f2_fma(dy0, dy0, d20);
+                        d21 = f2_fma(dy1, dy1, d21);
+                        d20 = f2_fma(dz0, dz0, d20);
+                        d21 = f2_fma(dz1, dz1, d21);
+                        float u0, v0, u1, v1;
+                        f2_unpack(d20, u0, v0);
+                        f2_unpack(d21, u1, v1);
+                        const f2 inv0 = f2_pack(rsqrt_hw(u0), rsqrt_hw(v0));
+                        const f2 inv1 = f2_pack(rsqrt_hw(u1), rsqrt_hw(v1));
+                        const f2 tm0 = f2_mul(mj0, inv0), tm1 = f2_mul(mj1, inv1);
+                        const f2 iq0 = f2_mul(inv0, inv0), iq1 = f2_mul(inv1, inv1);
+                        const f2 s0 = f2_mul(tm0, iq0), s1 = f2_mul(tm1, iq1);
+                        ax[q] = f2_fma(s0, dx0, ax[q]);
+                        ay[q] = f2_fma(s0, dy0, ay[q]);
+                        az[q] = f2_fma(s0, dz0, az[q]);
+                        ax[q] = f2_fma(s1, dx1, ax[q]);
+                        ay[q] = f2_fma(s1, dy1, ay[q]);
+                        az[q] = f2_fma(s1, dz1, az[q]);
+                        if (POT) pp[q] = f2_add(pp[q], f2_add(tm0, tm1));
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < KP; ++q) {
+                    tot.fold(q, 0, ax[q]);
+                    tot.fold(q, 1, ay[q]);
+                    tot.fold(q, 2, az[q]);
+                }
+            }
+        } else {
 #pragma unroll 1
         for (int jb = 0; jb < P; jb += kFoldJ) {
-#pragma unroll 8
+#pragma unroll U
             for (int jj = jb; jj < jb + kFoldJ; ++jj) {
                 const float4 a = s4[2 * jj];       // x, x, y, y
                 const float4 b = s4[2 * jj + 1];   // z, z, m, m
@@ -163,14 +309,15 @@ forces_tiled_kernel(const float *__restrict__ pm, int n, float eps2, int num_ib,
             }
 #pragma unroll
             for (int q = 0; q < KP; ++q) {
-                f2_kahan_fold(hx[q], lx[q], ax[q]);
-                f2_kahan_fold(hy[q], ly[q], ay[q]);
-                f2_kahan_fold(hz[q], lz[q], az[q]);
+                tot.fold(q, 0, ax[q]);
+                tot.fold(q, 1, ay[q]);
+                tot.fold(q, 2, az[q]);
             }
+        }
         }
         if (POT && ((k + 1) % FOLD_P == 0 || t + 1 == t_end)) {
 #pragma unroll
-            for (int q = 0; q < KP; ++q) f2_kahan_fold(hp[q], lp[q], pp[q]);
+            for (int q = 0; q < KP; ++q) tot.fold(q, 3, pp[q]);
         }
         stage = (stage + 1 == kStages) ? 0 : stage + 1;
     }
@@ -180,10 +327,10 @@ forces_tiled_kernel(const float *__restrict__ pm, int n, float eps2, int num_ib,
 #pragma unroll
     for (int q = 0; q < KP; ++q) {
         float x0, x1, y0, y1, z0, z1, p0 = 0.f, p1 = 0.f;
-        f2_unpack(f2_sub(hx[q], lx[q]), x0, x1);
-        f2_unpack(f2_sub(hy[q], ly[q]), y0, y1);
-        f2_unpack(f2_sub(hz[q], lz[q]), z0, z1);
-        if (POT) f2_unpack(f2_sub(hp[q], lp[q]), p0, p1);
+        f2_unpack(tot.value(q, 0), x0, x1);
+        f2_unpack(tot.value(q, 1), y0, y1);
+        f2_unpack(tot.value(q, 2), z0, z1);
+        if (POT) f2_unpack(tot.value(q, 3), p0, p1);
         const int64_t i0 = ibase + (2 * q) * NT;
         const int64_t i1 = ibase + (2 * q + 1) * NT;
         if (i0 < n) dst[i0] = make_float4(x0, y0, z0, -p0);
@@ -212,25 +359,43 @@ __global__ void reduce_splits_kernel(const float4 *__restrict__ part, int n, int
     }
 }
 
-#define NBODY_TILED(K, NT, P) {K, NT, P, reinterpret_cast<const void *>(&forces_tiled_kernel<K, NT, P, true>)}
+// Instantiated shapes: K targets per thread, NT threads, P-body tiles, the
+// minimum resident CTAs per SM asked of the register allocator, where the
+// compensated totals live (true: shared memory), the unroll factor U and the
+// loop MODE.  Variant 0 is the default: the fastest on GB300 from N = 2^18
+// to 2^20 (2.50e12 pairs/s at N = 2^20; packed FMA with three fresh
+// operands tops out near 90 % of the pipe, and this reaches about 89 % of
+// that).  The others stay selectable for tuning and tests.
+#define NBODY_TILED_LIST(X)                                 \
+    X(4, 256, 128, 2, true, 4, 2)   /* 0: default */         \
+    X(4, 256, 128, 2, false, 8, 0)  /* 1 */                  \
+    X(4, 128, 128, 5, false, 8, 0)  /* 2 */                  \
+    X(2, 128, 128, 8, false, 8, 0)  /* 3 */                  \
+    X(8, 128, 128, 3, false, 8, 0)  /* 4 */                  \
+    X(4, 256, 128, 3, true, 8, 0)   /* 5 */                  \
+    X(4, 256, 128, 2, false, 8, 1)  /* 6 */                  \
+    X(2, 256, 128, 4, false, 4, 2)  /* 7 */
 
-const TiledVariant kVariants[] = {
-    NBODY_TILED(4, 128, 128),   // 0: default
-    NBODY_TILED(8, 128, 128),   // 1
-    NBODY_TILED(2, 128, 128),   // 2
-    NBODY_TILED(4, 256, 128),   // 3
-};
+#define NBODY_TILED_ENTRY(K, NT, P, MINB, TS, U, MODE) \
+    {K, NT, P, reinterpret_cast<const void *>(&forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, true>)},
 
-#undef NBODY_TILED
+const TiledVariant kVariants[] = {NBODY_TILED_LIST(NBODY_TILED_ENTRY)};
 
-template <int K, int NT, int P>
+template <int K, int NT, int P, int MINB, bool TS, int U, int MODE>
 cudaError_t launch_variant(const float *pm, int n, float eps2, int num_ib, int splits, int tps,
                            int ntiles, float4 *out, cudaStream_t stream) {
     const unsigned grid = static_cast<unsigned>(num_ib) * static_cast<unsigned>(splits);
-    forces_tiled_kernel<K, NT, P, true><<<grid, NT, 0, stream>>>(pm, n, eps2, num_ib, tps,
-                                                                 ntiles, out);
+    forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, true><<<grid, NT, 0, stream>>>(
+        pm, n, eps2, num_ib, tps, ntiles, out);
     return cudaGetLastError();
 }
+
+typedef cudaError_t (*TiledLauncher)(const float *, int, float, int, int, int, int, float4 *,
+                                     cudaStream_t);
+
+#define NBODY_TILED_LAUNCHER(K, NT, P, MINB, TS, U, MODE) &launch_variant<K, NT, P, MINB, TS, U, MODE>,
+
+const TiledLauncher kLaunchers[] = {NBODY_TILED_LIST(NBODY_TILED_LAUNCHER)};
 
 }  // namespace
 
@@ -240,13 +405,8 @@ const TiledVariant &tiled_variant(int v) { return kVariants[v]; }
 
 cudaError_t launch_tiled(int variant, const float *pm, int n, float eps2, int num_ib, int splits,
                          int tps, int ntiles, float4 *out, cudaStream_t stream) {
-    switch (variant) {
-        case 0: return launch_variant<4, 128, 128>(pm, n, eps2, num_ib, splits, tps, ntiles, out, stream);
-        case 1: return launch_variant<8, 128, 128>(pm, n, eps2, num_ib, splits, tps, ntiles, out, stream);
-        case 2: return launch_variant<2, 128, 128>(pm, n, eps2, num_ib, splits, tps, ntiles, out, stream);
-        case 3: return launch_variant<4, 256, 128>(pm, n, eps2, num_ib, splits, tps, ntiles, out, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    if (variant < 0 || variant >= tiled_variant_count()) return cudaErrorInvalidValue;
+    return kLaunchers[variant](pm, n, eps2, num_ib, splits, tps, ntiles, out, stream);
 }
 
 cudaError_t launch_reduce_splits(const float4 *part, int n, int splits, float4 *out, int sm_count,

@@ -46,12 +46,13 @@ nbody_status check_forces(const float *pm, int64_t n, float eps2, const float *a
 // ---------------------------------------------------------------- per-device state
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxVariants = 32;
 
 struct DeviceState {
     bool ready = false;
     int sm_count = 0;
-    int tiled_occ[8] = {0};
-    int cluster_occ[8] = {0};
+    int tiled_occ[kMaxVariants] = {0};
+    int cluster_occ[kMaxVariants] = {0};
     cudaMemPool_t pool = nullptr;     // stream-ordered scratch for split partials
 };
 
@@ -72,13 +73,13 @@ nbody_status device_state(DeviceState **out) {
             (e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return cuda_fail(e);
         if (major != 10 || minor != 3) return NBODY_ERR_DEVICE;   // built for sm_103a only
-        for (int v = 0; v < nbody::tiled_variant_count() && v < 8; ++v) {
+        for (int v = 0; v < nbody::tiled_variant_count() && v < kMaxVariants; ++v) {
             const nbody::TiledVariant &tv = nbody::tiled_variant(v);
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.tiled_occ[v], tv.fn_pot,
                                                               tv.threads, 0);
             if (e != cudaSuccess) return cuda_fail(e);
         }
-        for (int v = 0; v < nbody::cluster_variant_count() && v < 8; ++v) {
+        for (int v = 0; v < nbody::cluster_variant_count() && v < kMaxVariants; ++v) {
             const nbody::ClusterVariant &cv = nbody::cluster_variant(v);
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.cluster_occ[v], cv.fn_pot,
                                                               cv.warps * 32, 0);
@@ -206,8 +207,9 @@ void plan_cluster_variant(int64_t n, int sm, int occ, int variant, nbody_plan *p
 }
 
 // Largest n the automatic choice sends to the cluster path (measured on
-// GB300: the cluster path is ahead up to 8192 bodies, the tiled one from 12288).
-constexpr int64_t kClusterMaxN = 10240;
+// GB300 inside CUDA graphs: the cluster path is ahead up to 4096 bodies, the
+// tiled one from 8192).
+constexpr int64_t kClusterMaxN = 6144;
 
 nbody_status make_plan(int64_t n, int sm, const int *tiled_occ, const int *cluster_occ,
                        const nbody_forces_opts *opts, nbody_plan *p) {
@@ -220,7 +222,8 @@ nbody_status make_plan(int64_t n, int sm, const int *tiled_occ, const int *clust
     if (path == NBODY_PATH_AUTO) path = n <= kClusterMaxN ? NBODY_PATH_CLUSTER : NBODY_PATH_TILED;
     if (path == NBODY_PATH_TILED) {
         const int variant = o.variant < 0 ? kDefaultTiledVariant : o.variant;
-        if (variant >= nbody::tiled_variant_count()) return NBODY_ERR_INVALID_ARG;
+        if (variant >= nbody::tiled_variant_count() || variant >= kMaxVariants)
+            return NBODY_ERR_INVALID_ARG;
         plan_tiled(n, sm, tiled_occ[variant], variant, o.splits, p);
         return NBODY_OK;
     }
@@ -273,12 +276,12 @@ int nbody_last_cuda_error(void) { return g_last_cuda_error; }
 
 nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
                                const nbody_forces_opts *opts, nbody_plan *plan) {
-    int occ[8], cocc[8];
-    for (int v = 0; v < nbody::tiled_variant_count() && v < 8; ++v) {
+    int occ[kMaxVariants], cocc[kMaxVariants];
+    for (int v = 0; v < nbody::tiled_variant_count() && v < kMaxVariants; ++v) {
         const nbody::TiledVariant &tv = nbody::tiled_variant(v);
         occ[v] = ctas_per_sm > 0 ? ctas_per_sm : nominal_occ(tv.i_per_thread, tv.threads);
     }
-    for (int v = 0; v < nbody::cluster_variant_count() && v < 8; ++v) {
+    for (int v = 0; v < nbody::cluster_variant_count() && v < kMaxVariants; ++v) {
         const nbody::ClusterVariant &cv = nbody::cluster_variant(v);
         cocc[v] = ctas_per_sm > 0 ? ctas_per_sm : nominal_occ(cv.i_per_thread, cv.warps * 32);
     }

@@ -139,7 +139,8 @@ def test_cluster_plan_covers_all_pairs(n, variant):
 
 def test_auto_path_choice():
     assert apg.nbody_plan_forces(1024, 152)["path"] == apg.NBODY_PATH_CLUSTER
-    assert apg.nbody_plan_forces(8192, 152)["path"] == apg.NBODY_PATH_CLUSTER
+    assert apg.nbody_plan_forces(4096, 152)["path"] == apg.NBODY_PATH_CLUSTER
+    assert apg.nbody_plan_forces(8192, 152)["path"] == apg.NBODY_PATH_TILED
     assert apg.nbody_plan_forces(1048576, 152)["path"] == apg.NBODY_PATH_TILED
     with pytest.raises(apg.NbodyError):
         apg.nbody_plan_forces(1000, 152, path=apg.NBODY_PATH_CLUSTER, splits=3)
@@ -148,7 +149,15 @@ def test_auto_path_choice():
 
 
 def test_plan_forced_splits_and_variants(lib):
-    for v in range(4):
+    v = 0
+    while True:
+        try:
+            apg.nbody_plan_forces(1000, 152, path=apg.NBODY_PATH_TILED, variant=v)
+        except apg.NbodyError:
+            break
+        v += 1
+    assert v >= 4
+    for v in range(v):
         for s in (1, 2, 7, 64):
             plan = apg.nbody_plan_forces(200003, 152, path=apg.NBODY_PATH_TILED, variant=v,
                                          splits=s)
