@@ -27,7 +27,8 @@ NBODY_NOALLOC_MAX_N = 4194304
 
 # Every symbol include/nbody.h declares (checked by the tests).
 EXPORTS = ["nbody_forces", "nbody_euler_step", "nbody_status_string", "nbody_last_cuda_error",
-           "nbody_plan_forces", "nbody_forces_ex", "nbody_forces_noalloc"]
+           "nbody_plan_forces", "nbody_forces_ex", "nbody_forces_noalloc", "nbody_forces_ts",
+           "nbody_simulate"]
 
 
 class nbody_forces_opts(ctypes.Structure):
@@ -69,6 +70,10 @@ _SIGS = {
     "nbody_last_cuda_error": ([], ctypes.c_int),
     "nbody_plan_forces": ([ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P], ctypes.c_int),
     "nbody_forces_noalloc": ([_P, ctypes.c_int64, ctypes.c_float, _P, _P], ctypes.c_int),
+    "nbody_forces_ts": ([_P, ctypes.c_int64, _P, ctypes.c_int64, ctypes.c_float, _P, _P],
+                        ctypes.c_int),
+    "nbody_simulate": ([_P, _P, _P, ctypes.c_int64, ctypes.c_float, ctypes.c_float,
+                        ctypes.c_int64, _P], ctypes.c_int),
 }
 
 
@@ -152,6 +157,27 @@ def nbody_forces_ex(pos_mass, eps2, acc_pot=None, path=NBODY_PATH_AUTO, variant=
     return acc_pot
 
 
+def nbody_forces_ts(targets, sources, eps2, out=None, stream=None):
+    """(ax, ay, az, p) at each target from every source, as a new or the given
+    [nt, 4] tensor."""
+    import torch
+    lib = load_library()
+    _bodies(targets, "targets")
+    _bodies(sources, "sources")
+    nt, ns = targets.shape[0], sources.shape[0]
+    if out is None:
+        out = torch.empty_like(targets)
+    _bodies(out, "out", nt)
+    if not (targets.device == sources.device == out.device):
+        raise ValueError("targets, sources and out must be on the same device")
+    with torch.cuda.device(targets.device):
+        st = lib.nbody_forces_ts(_ptr(targets), nt, _ptr(sources), ns, ctypes.c_float(float(eps2)),
+                                 _ptr(out), _stream_handle(targets.device, stream))
+    if st != 0:
+        raise NbodyError(st, "nbody_forces_ts")
+    return out
+
+
 def nbody_forces_noalloc(pos_mass, eps2, acc_pot, stream=None):
     """nbody_forces computed with the library's fixed scratch: the C call
     allocates nothing, so acc_pot must be given (n <= NBODY_NOALLOC_MAX_N)."""
@@ -186,6 +212,24 @@ def nbody_euler_step(pos_mass, vel, acc_pot, dt, stream=None):
                                   _stream_handle(pos_mass.device, stream))
     if st != 0:
         raise NbodyError(st, "nbody_euler_step")
+
+
+def nbody_simulate(pos_mass, vel, acc_pot, eps2, dt, steps, stream=None):
+    """`steps` device-resident force + Euler steps, in place (CUDA-graph replay)."""
+    import torch
+    lib = load_library()
+    _bodies(pos_mass, "pos_mass")
+    n = pos_mass.shape[0]
+    _bodies(vel, "vel", n)
+    _bodies(acc_pot, "acc_pot", n)
+    if not (pos_mass.device == vel.device == acc_pot.device):
+        raise ValueError("pos_mass, vel and acc_pot must be on the same device")
+    with torch.cuda.device(pos_mass.device):
+        st = lib.nbody_simulate(_ptr(pos_mass), _ptr(vel), _ptr(acc_pot), n,
+                                ctypes.c_float(float(eps2)), ctypes.c_float(float(dt)), int(steps),
+                                _stream_handle(pos_mass.device, stream))
+    if st != 0:
+        raise NbodyError(st, "nbody_simulate")
 
 
 def nbody_plan_forces(n, sm_count, ctas_per_sm=0, path=NBODY_PATH_AUTO, variant=-1, splits=0):

@@ -61,7 +61,7 @@ __device__ __forceinline__ float4 ld_dsmem_f4(const void *local, uint32_t rank) 
 }
 
 template <int NT, int P>
-__device__ __forceinline__ void stage_tile(float *sbuf, const float *pm, int n, int tile) {
+__device__ __forceinline__ void stage_tile(float *sbuf, const float *src_bodies, int ns, int tile) {
     static_assert((8 * P) % NT == 0, "tile copies must divide evenly among threads");
     const uint32_t sbase = smem_u32(sbuf);
     const int64_t j0 = static_cast<int64_t>(tile) * P;
@@ -70,8 +70,8 @@ __device__ __forceinline__ void stage_tile(float *sbuf, const float *pm, int n, 
         const int idx = r * NT + static_cast<int>(threadIdx.x);
         const int64_t j = j0 + (idx >> 3);
         const int comp = (idx >> 1) & 3;
-        const bool ok = j < n;
-        const float *src = pm + (ok ? j * 4 + comp : 0);
+        const bool ok = j < ns;
+        const float *src = src_bodies + (ok ? j * 4 + comp : 0);
         cp_async_4(sbase + 4u * static_cast<uint32_t>(idx), src, ok ? 4 : 0);
     }
 }
@@ -85,8 +85,8 @@ __device__ __forceinline__ void kahan1(float &hi, float &lo, float x) {
 
 template <int K, int W, int P, bool POT>
 __global__ void __launch_bounds__(W * 32)
-forces_cluster_kernel(const float *__restrict__ pm, int n, float eps2, int tiles_per_cta,
-                      int ntiles, float4 *__restrict__ out) {
+forces_cluster_kernel(const Problem pr, int tiles_per_cta, int ntiles,
+                      float4 *__restrict__ out) {
     static_assert(K % 2 == 0, "targets are processed in f32x2 pairs");
     constexpr int KP = K / 2;
     constexpr int NT = W * 32;
@@ -107,20 +107,21 @@ forces_cluster_kernel(const float *__restrict__ pm, int n, float eps2, int tiles
     const int t_begin = static_cast<int>(crank) * tiles_per_cta;
     const int t_end = min(t_begin + tiles_per_cta, ntiles);
     const int64_t ibase = static_cast<int64_t>(ib) * BI + lane;
-    const float4 *pm4 = reinterpret_cast<const float4 *>(pm);
+    const float4 *tg4 = reinterpret_cast<const float4 *>(pr.targets);
+    const int n = pr.nt;   // targets
 
     f2 xi[KP], yi[KP], zi[KP];
 #pragma unroll
     for (int q = 0; q < KP; ++q) {
         const int64_t i0 = min(ibase + (2 * q) * 32, static_cast<int64_t>(n) - 1);
         const int64_t i1 = min(ibase + (2 * q + 1) * 32, static_cast<int64_t>(n) - 1);
-        const float4 b0 = __ldg(pm4 + i0);
-        const float4 b1 = __ldg(pm4 + i1);
+        const float4 b0 = __ldg(tg4 + i0);
+        const float4 b1 = __ldg(tg4 + i1);
         xi[q] = f2_pack(b0.x, b1.x);
         yi[q] = f2_pack(b0.y, b1.y);
         zi[q] = f2_pack(b0.z, b1.z);
     }
-    const f2 e2 = f2_pack(eps2, eps2);
+    const f2 e2 = f2_pack(pr.eps2, pr.eps2);
 
     f2 ax[KP], ay[KP], az[KP], pp[KP];
     f2 hx[KP], hy[KP], hz[KP], hp[KP];
@@ -132,9 +133,9 @@ forces_cluster_kernel(const float *__restrict__ pm, int n, float eps2, int tiles
         lx[q] = ly[q] = lz[q] = lp[q] = 0ull;
     }
 
-    if (t_begin < t_end) stage_tile<NT, P>(sdup[0], pm, n, t_begin);
+    if (t_begin < t_end) stage_tile<NT, P>(sdup[0], pr.sources, pr.ns, t_begin);
     cp_async_commit();
-    if (t_begin + 1 < t_end) stage_tile<NT, P>(sdup[1], pm, n, t_begin + 1);
+    if (t_begin + 1 < t_end) stage_tile<NT, P>(sdup[1], pr.sources, pr.ns, t_begin + 1);
     cp_async_commit();
 
     int stage = 0;
@@ -145,7 +146,7 @@ forces_cluster_kernel(const float *__restrict__ pm, int n, float eps2, int tiles
         {
             int s2 = stage + 2;
             if (s2 >= kStages) s2 -= kStages;
-            if (t + 2 < t_end) stage_tile<NT, P>(sdup[s2], pm, n, t + 2);
+            if (t + 2 < t_end) stage_tile<NT, P>(sdup[s2], pr.sources, pr.ns, t + 2);
             cp_async_commit();
         }
         const float4 *s4 = reinterpret_cast<const float4 *>(sdup[stage]) + 2 * (warp * JW);
@@ -257,8 +258,8 @@ const ClusterVariant kVariants[] = {
 #undef NBODY_CLUSTER
 
 template <int K, int W, int P>
-cudaError_t launch_variant(const float *pm, int n, float eps2, int num_ib, int cluster, int tpc,
-                           int ntiles, float4 *out, cudaStream_t stream) {
+cudaError_t launch_variant(const Problem &pr, int num_ib, int cluster, int tpc, int ntiles,
+                           float4 *out, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_ib) * static_cast<unsigned>(cluster), 1, 1);
     cfg.blockDim = dim3(W * 32, 1, 1);
@@ -271,8 +272,7 @@ cudaError_t launch_variant(const float *pm, int n, float eps2, int num_ib, int c
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true>, pm, n, eps2, tpc, ntiles,
-                              out);
+    return cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true>, pr, tpc, ntiles, out);
 }
 
 }  // namespace
@@ -281,13 +281,13 @@ int cluster_variant_count() { return static_cast<int>(sizeof(kVariants) / sizeof
 
 const ClusterVariant &cluster_variant(int v) { return kVariants[v]; }
 
-cudaError_t launch_cluster(int variant, const float *pm, int n, float eps2, int num_ib, int cluster,
+cudaError_t launch_cluster(int variant, const Problem &pr, int num_ib, int cluster,
                            int tiles_per_cta, int ntiles, float4 *out, cudaStream_t stream) {
     switch (variant) {
-        case 0: return launch_variant<2, 4, 128>(pm, n, eps2, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
-        case 1: return launch_variant<4, 4, 128>(pm, n, eps2, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
-        case 2: return launch_variant<2, 8, 128>(pm, n, eps2, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
-        case 3: return launch_variant<4, 8, 128>(pm, n, eps2, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        case 0: return launch_variant<2, 4, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        case 1: return launch_variant<4, 4, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        case 2: return launch_variant<2, 8, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        case 3: return launch_variant<4, 8, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
         default: return cudaErrorInvalidValue;
     }
 }

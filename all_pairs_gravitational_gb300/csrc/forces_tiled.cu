@@ -54,7 +54,7 @@ constexpr int kFoldJ = 32;
 // the duplicated layout.  Each 4-byte copy moves one component into one of
 // its two slots; bodies past n are written as zeros.
 template <int NT, int P>
-__device__ __forceinline__ void stage_tile(float *sbuf, const float *pm, int n, int tile) {
+__device__ __forceinline__ void stage_tile(float *sbuf, const float *src_bodies, int ns, int tile) {
     static_assert((8 * P) % NT == 0, "tile copies must divide evenly among threads");
     const uint32_t sbase = smem_u32(sbuf);
     const int64_t j0 = static_cast<int64_t>(tile) * P;
@@ -63,8 +63,8 @@ __device__ __forceinline__ void stage_tile(float *sbuf, const float *pm, int n, 
         const int idx = r * NT + static_cast<int>(threadIdx.x);   // float slot in the tile
         const int64_t j = j0 + (idx >> 3);
         const int comp = (idx >> 1) & 3;
-        const bool ok = j < n;
-        const float *src = pm + (ok ? j * 4 + comp : 0);
+        const bool ok = j < ns;
+        const float *src = src_bodies + (ok ? j * 4 + comp : 0);
         cp_async_4(sbase + 4u * static_cast<uint32_t>(idx), src, ok ? 4 : 0);
     }
 }
@@ -114,8 +114,8 @@ struct Totals<KP, NT, true> {
 // per step, their instructions interleaved in source order.
 template <int K, int NT, int P, int MINB, bool TSMEM, int U, int MODE, bool POT>
 __global__ void __launch_bounds__(NT, MINB)
-forces_tiled_kernel(const float *__restrict__ pm, int n, float eps2, int num_ib,
-                    int tiles_per_split, int ntiles, float4 *__restrict__ out) {
+forces_tiled_kernel(const Problem pr, int num_ib, int tiles_per_split, int ntiles,
+                    float4 *__restrict__ out) {
     static_assert(K % 2 == 0, "targets are processed in f32x2 pairs");
     constexpr int KP = K / 2;
     constexpr int FOLD_P = (1024 + P - 1) / P;   // tiles between folds of the potential
@@ -133,7 +133,8 @@ forces_tiled_kernel(const float *__restrict__ pm, int n, float eps2, int num_ib,
     const int t_begin = split * tiles_per_split;
     const int t_end = min(t_begin + tiles_per_split, ntiles);
     const int64_t ibase = static_cast<int64_t>(ib) * (NT * K) + tid;
-    const float4 *pm4 = reinterpret_cast<const float4 *>(pm);
+    const float4 *tg4 = reinterpret_cast<const float4 *>(pr.targets);
+    const int n = pr.nt;   // targets
 
     // Targets: lane 0 of pair q is body ibase + 2q*NT, lane 1 is ibase + (2q+1)*NT.
     f2 xi[KP], yi[KP], zi[KP];
@@ -141,13 +142,13 @@ forces_tiled_kernel(const float *__restrict__ pm, int n, float eps2, int num_ib,
     for (int q = 0; q < KP; ++q) {
         const int64_t i0 = min(ibase + (2 * q) * NT, static_cast<int64_t>(n) - 1);
         const int64_t i1 = min(ibase + (2 * q + 1) * NT, static_cast<int64_t>(n) - 1);
-        const float4 b0 = __ldg(pm4 + i0);
-        const float4 b1 = __ldg(pm4 + i1);
+        const float4 b0 = __ldg(tg4 + i0);
+        const float4 b1 = __ldg(tg4 + i1);
         xi[q] = f2_pack(b0.x, b1.x);
         yi[q] = f2_pack(b0.y, b1.y);
         zi[q] = f2_pack(b0.z, b1.z);
     }
-    const f2 e2 = f2_pack(eps2, eps2);
+    const f2 e2 = f2_pack(pr.eps2, pr.eps2);
 
     f2 ax[KP], ay[KP], az[KP], pp[KP];          // fp32 partials of the current fold
 #pragma unroll
@@ -160,9 +161,9 @@ forces_tiled_kernel(const float *__restrict__ pm, int n, float eps2, int num_ib,
     tot.init();
 
     // Prologue: two tiles in flight (one commit group per tile, empty past the end).
-    if (t_begin < t_end) stage_tile<NT, P>(sdup[0], pm, n, t_begin);
+    if (t_begin < t_end) stage_tile<NT, P>(sdup[0], pr.sources, pr.ns, t_begin);
     cp_async_commit();
-    if (t_begin + 1 < t_end) stage_tile<NT, P>(sdup[1], pm, n, t_begin + 1);
+    if (t_begin + 1 < t_end) stage_tile<NT, P>(sdup[1], pr.sources, pr.ns, t_begin + 1);
     cp_async_commit();
 
     int stage = 0;
@@ -173,7 +174,7 @@ forces_tiled_kernel(const float *__restrict__ pm, int n, float eps2, int num_ib,
         {
             int s2 = stage + 2;
             if (s2 >= kStages) s2 -= kStages;
-            if (t + 2 < t_end) stage_tile<NT, P>(sdup[s2], pm, n, t + 2);
+            if (t + 2 < t_end) stage_tile<NT, P>(sdup[s2], pr.sources, pr.ns, t + 2);
             cp_async_commit();
         }
 
@@ -382,16 +383,15 @@ __global__ void reduce_splits_kernel(const float4 *__restrict__ part, int n, int
 const TiledVariant kVariants[] = {NBODY_TILED_LIST(NBODY_TILED_ENTRY)};
 
 template <int K, int NT, int P, int MINB, bool TS, int U, int MODE>
-cudaError_t launch_variant(const float *pm, int n, float eps2, int num_ib, int splits, int tps,
-                           int ntiles, float4 *out, cudaStream_t stream) {
+cudaError_t launch_variant(const Problem &pr, int num_ib, int splits, int tps, int ntiles,
+                           float4 *out, cudaStream_t stream) {
     const unsigned grid = static_cast<unsigned>(num_ib) * static_cast<unsigned>(splits);
     forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, true><<<grid, NT, 0, stream>>>(
-        pm, n, eps2, num_ib, tps, ntiles, out);
+        pr, num_ib, tps, ntiles, out);
     return cudaGetLastError();
 }
 
-typedef cudaError_t (*TiledLauncher)(const float *, int, float, int, int, int, int, float4 *,
-                                     cudaStream_t);
+typedef cudaError_t (*TiledLauncher)(const Problem &, int, int, int, int, float4 *, cudaStream_t);
 
 #define NBODY_TILED_LAUNCHER(K, NT, P, MINB, TS, U, MODE) &launch_variant<K, NT, P, MINB, TS, U, MODE>,
 
@@ -403,10 +403,10 @@ int tiled_variant_count() { return static_cast<int>(sizeof(kVariants) / sizeof(k
 
 const TiledVariant &tiled_variant(int v) { return kVariants[v]; }
 
-cudaError_t launch_tiled(int variant, const float *pm, int n, float eps2, int num_ib, int splits,
-                         int tps, int ntiles, float4 *out, cudaStream_t stream) {
+cudaError_t launch_tiled(int variant, const Problem &pr, int num_ib, int splits, int tps,
+                         int ntiles, float4 *out, cudaStream_t stream) {
     if (variant < 0 || variant >= tiled_variant_count()) return cudaErrorInvalidValue;
-    return kLaunchers[variant](pm, n, eps2, num_ib, splits, tps, ntiles, out, stream);
+    return kLaunchers[variant](pr, num_ib, splits, tps, ntiles, out, stream);
 }
 
 cudaError_t launch_reduce_splits(const float4 *part, int n, int splits, float4 *out, int sm_count,

@@ -3,7 +3,9 @@
 #include <cfloat>
 #include <climits>
 #include <cmath>
+#include <algorithm>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "nbody.h"
@@ -27,6 +29,13 @@ bool overlap(const void *a, const void *b, int64_t bytes) {
     const uintptr_t y = reinterpret_cast<uintptr_t>(b);
     const uintptr_t len = static_cast<uintptr_t>(bytes);
     return x < y + len && y < x + len;
+}
+
+// [a, a + a_bytes) and [b, b + b_bytes) share a byte.
+bool overlap2(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a);
+    const uintptr_t y = reinterpret_cast<uintptr_t>(b);
+    return x < y + static_cast<uintptr_t>(b_bytes) && y < x + static_cast<uintptr_t>(a_bytes);
 }
 
 nbody_status check_n(int64_t n) {
@@ -102,7 +111,7 @@ nbody_status device_state(DeviceState **out) {
 // ---------------------------------------------------------------- planner
 
 constexpr int kDefaultTiledVariant = 0;
-constexpr int kMaxSplits = 256;
+constexpr int kMaxSplits = 1024;
 constexpr int64_t kMaxScratchBytes = int64_t(2) << 30;
 // Relative cost model (only ratios matter): pair rate of one SM, the fixed
 // cost of a work item in source-body equivalents, one launch, scratch traffic.
@@ -113,16 +122,17 @@ constexpr double kScratchBytesPerSecond = 5.0e12;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-void plan_tiled(int64_t n, int sm, int occ, int variant, int splits_req, nbody_plan *p) {
+void plan_tiled(int64_t nt, int64_t ns, int sm, int occ, int variant, int splits_req,
+                nbody_plan *p) {
     const nbody::TiledVariant &v = nbody::tiled_variant(variant);
     const int64_t bi = static_cast<int64_t>(v.threads) * v.i_per_thread;
-    const int64_t num_ib = ceil_div(n, bi);
-    const int64_t ntiles = ceil_div(n, v.tile);
+    const int64_t num_ib = ceil_div(nt, bi);
+    const int64_t ntiles = ceil_div(ns, v.tile);
     const int64_t slots = static_cast<int64_t>(sm > 0 ? sm : 1) * (occ > 0 ? occ : 1);
     const double slot_rate = kPairsPerSmSecond / (occ > 0 ? occ : 1);
 
     int64_t s_lo = 1, s_hi = std::min<int64_t>(ntiles, kMaxSplits);
-    s_hi = std::max<int64_t>(1, std::min<int64_t>(s_hi, kMaxScratchBytes / (16 * n)));
+    s_hi = std::max<int64_t>(1, std::min<int64_t>(s_hi, kMaxScratchBytes / (16 * nt)));
     if (splits_req > 0) s_lo = s_hi = std::min<int64_t>(splits_req, ntiles);
 
     double best_t = INFINITY;
@@ -135,7 +145,7 @@ void plan_tiled(int64_t n, int sm, int occ, int variant, int splits_req, nbody_p
         const int64_t waves = ceil_div(items, slots);
         double t = static_cast<double>(waves) *
                    static_cast<double>(tps * v.tile + kItemOverheadBodies) * bi / slot_rate;
-        if (used > 1) t += kLaunchSeconds + 32.0 * used * n / kScratchBytesPerSecond;
+        if (used > 1) t += kLaunchSeconds + 32.0 * used * nt / kScratchBytesPerSecond;
         if (t < best_t * (1.0 - 1e-3)) {
             best_t = t;
             best_s = used;
@@ -154,7 +164,7 @@ void plan_tiled(int64_t n, int sm, int occ, int variant, int splits_req, nbody_p
     p->cluster = 1;
     p->warps_j = 1;
     p->grid = num_ib * best_s;
-    p->scratch_bytes = best_s > 1 ? 16 * best_s * n : 0;
+    p->scratch_bytes = best_s > 1 ? 16 * best_s * nt : 0;
     p->fill = static_cast<double>(num_ib * best_s) / static_cast<double>(best_waves * slots);
 }
 
@@ -164,11 +174,12 @@ void plan_tiled(int64_t n, int sm, int occ, int variant, int splits_req, nbody_p
 // full pair rate with kWarpsToSaturate resident warps.
 constexpr int kWarpsToSaturate = 16;
 
-void plan_cluster_variant(int64_t n, int sm, int occ, int variant, nbody_plan *p, double *t_out) {
+void plan_cluster_variant(int64_t nt, int64_t ns, int sm, int occ, int variant, nbody_plan *p,
+                          double *t_out) {
     const nbody::ClusterVariant &v = nbody::cluster_variant(variant);
     const int64_t bi = 32LL * v.i_per_thread;
-    const int64_t num_ib = ceil_div(n, bi);
-    const int64_t ntiles = ceil_div(n, v.tile);
+    const int64_t num_ib = ceil_div(nt, bi);
+    const int64_t ntiles = ceil_div(ns, v.tile);
     double best_t = INFINITY;
     int64_t best_c = 1, best_tpc = ntiles;
     double best_fill = 0.0;
@@ -211,20 +222,22 @@ void plan_cluster_variant(int64_t n, int sm, int occ, int variant, nbody_plan *p
 // tiled one from 8192).
 constexpr int64_t kClusterMaxN = 6144;
 
-nbody_status make_plan(int64_t n, int sm, const int *tiled_occ, const int *cluster_occ,
-                       const nbody_forces_opts *opts, nbody_plan *p) {
-    if (n <= 0 || n > INT32_MAX || sm <= 0 || p == nullptr) return NBODY_ERR_INVALID_ARG;
+nbody_status make_plan(int64_t nt, int64_t ns, int sm, const int *tiled_occ,
+                       const int *cluster_occ, const nbody_forces_opts *opts, nbody_plan *p) {
+    if (nt <= 0 || nt > INT32_MAX || ns <= 0 || ns > INT32_MAX || sm <= 0 || p == nullptr)
+        return NBODY_ERR_INVALID_ARG;
     nbody_forces_opts o = {NBODY_PATH_AUTO, -1, 0, 0};
     if (opts != nullptr) o = *opts;
     if (o.path < NBODY_PATH_AUTO || o.path > NBODY_PATH_CLUSTER || o.splits < 0)
         return NBODY_ERR_INVALID_ARG;
     int path = o.path;
-    if (path == NBODY_PATH_AUTO) path = n <= kClusterMaxN ? NBODY_PATH_CLUSTER : NBODY_PATH_TILED;
+    if (path == NBODY_PATH_AUTO)
+        path = (nt <= kClusterMaxN && ns <= kClusterMaxN) ? NBODY_PATH_CLUSTER : NBODY_PATH_TILED;
     if (path == NBODY_PATH_TILED) {
         const int variant = o.variant < 0 ? kDefaultTiledVariant : o.variant;
         if (variant >= nbody::tiled_variant_count() || variant >= kMaxVariants)
             return NBODY_ERR_INVALID_ARG;
-        plan_tiled(n, sm, tiled_occ[variant], variant, o.splits, p);
+        plan_tiled(nt, ns, sm, tiled_occ[variant], variant, o.splits, p);
         return NBODY_OK;
     }
     if (o.splits != 0) return NBODY_ERR_INVALID_ARG;   // the cluster path plans its own split
@@ -234,12 +247,154 @@ nbody_status make_plan(int64_t n, int sm, const int *tiled_occ, const int *clust
         if (o.variant >= 0 && v != o.variant) continue;
         nbody_plan cand;
         double t;
-        plan_cluster_variant(n, sm, cluster_occ[v], v, &cand, &t);
+        plan_cluster_variant(nt, ns, sm, cluster_occ[v], v, &cand, &t);
         if (t < best * (1.0 - 1e-3)) {
             best = t;
             *p = cand;
         }
     }
+    return NBODY_OK;
+}
+
+// Launch a planned force evaluation; `scratch` holds plan.scratch_bytes when
+// plan.splits > 1.
+cudaError_t launch_planned(const nbody_plan &plan, const nbody::Problem &pr, float4 *out,
+                           float4 *scratch, int sm_count, cudaStream_t stream) {
+    const int ntiles = static_cast<int>(ceil_div(pr.ns, plan.tile));
+    if (plan.path == NBODY_PATH_CLUSTER)
+        return nbody::launch_cluster(plan.variant, pr, plan.num_iblocks, plan.cluster,
+                                     plan.tiles_per_split, ntiles, out, stream);
+    if (plan.splits == 1)
+        return nbody::launch_tiled(plan.variant, pr, plan.num_iblocks, 1, plan.tiles_per_split,
+                                   ntiles, out, stream);
+    cudaError_t e = nbody::launch_tiled(plan.variant, pr, plan.num_iblocks, plan.splits,
+                                        plan.tiles_per_split, ntiles, scratch, stream);
+    if (e == cudaSuccess) e = nbody::launch_reduce_splits(scratch, pr.nt, plan.splits, out, sm_count, stream);
+    return e;
+}
+
+// Launch one planned force evaluation (targets x sources) on `stream`, with
+// its split partials in stream-ordered memory from the device's pool.
+nbody_status run_forces(const nbody::Problem &pr, const nbody_forces_opts *opts, float *result,
+                        cudaStream_t stream) {
+    DeviceState *dev = nullptr;
+    nbody_status st = device_state(&dev);
+    if (st != NBODY_OK) return st;
+    nbody_plan plan;
+    if ((st = make_plan(pr.nt, pr.ns, dev->sm_count, dev->tiled_occ, dev->cluster_occ, opts,
+                        &plan)) != NBODY_OK)
+        return st;
+    float4 *out = reinterpret_cast<float4 *>(result);
+    void *scratch = nullptr;
+    cudaError_t e;
+    if (plan.path == NBODY_PATH_TILED && plan.splits > 1) {
+        e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.scratch_bytes), dev->pool,
+                                    stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    e = launch_planned(plan, pr, out, static_cast<float4 *>(scratch), dev->sm_count, stream);
+    if (scratch != nullptr) {
+        const cudaError_t ef = cudaFreeAsync(scratch, stream);
+        if (e == cudaSuccess) e = ef;
+    }
+    return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------- multi-step driver
+//
+// One step (forces, then Euler) is captured once into a CUDA graph on an
+// internal stream and replayed `steps` times on the caller's stream, so a
+// step costs one graph launch instead of two or three kernel launches from
+// the host.  One graph per device is cached, keyed by every argument but the
+// step count; its split scratch (if any) lives as long as the graph.  When
+// the key changes, the old graph is destroyed (deferred until it finishes)
+// and its scratch freed in stream order behind its last launch.
+
+struct SimKey {
+    const float *pm;
+    float *vel;
+    float *acc;
+    int64_t n;
+    float eps2;
+    float dt;
+    bool operator==(const SimKey &o) const {
+        return pm == o.pm && vel == o.vel && acc == o.acc && n == o.n &&
+               std::memcmp(&eps2, &o.eps2, sizeof(float)) == 0 &&
+               std::memcmp(&dt, &o.dt, sizeof(float)) == 0;
+    }
+};
+
+struct SimGraph {
+    bool valid = false;
+    SimKey key = {};
+    cudaGraphExec_t exec = nullptr;
+    void *scratch = nullptr;
+    cudaEvent_t done = nullptr;    // recorded after the latest replay
+};
+
+std::mutex g_sim_mu;
+SimGraph g_sim[kMaxDevices];
+cudaStream_t g_capture[kMaxDevices] = {};
+
+nbody_status sim_release(SimGraph &g, cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    if (g.exec != nullptr) e = cudaGraphExecDestroy(g.exec);
+    if (g.scratch != nullptr) {
+        if (g.done != nullptr) cudaStreamWaitEvent(stream, g.done, 0);
+        const cudaError_t ef = cudaFreeAsync(g.scratch, stream);
+        if (e == cudaSuccess) e = ef;
+    }
+    g.exec = nullptr;
+    g.scratch = nullptr;
+    g.valid = false;
+    return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
+}
+
+nbody_status sim_build(int dev_id, DeviceState *dev, const SimKey &k, SimGraph &g,
+                       cudaStream_t stream) {
+    nbody_plan plan;
+    nbody_status st = make_plan(k.n, k.n, dev->sm_count, dev->tiled_occ, dev->cluster_occ,
+                                nullptr, &plan);
+    if (st != NBODY_OK) return st;
+    cudaError_t e;
+    if (g_capture[dev_id] == nullptr &&
+        (e = cudaStreamCreateWithFlags(&g_capture[dev_id], cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail(e);
+    if (g.done == nullptr && (e = cudaEventCreateWithFlags(&g.done, cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e);
+    void *scratch = nullptr;
+    if (plan.path == NBODY_PATH_TILED && plan.splits > 1) {
+        e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.scratch_bytes), dev->pool,
+                                    stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    const cudaStream_t cap = g_capture[dev_id];
+    const int ni = static_cast<int>(k.n);
+    const nbody::Problem pr = {k.pm, k.pm, ni, ni, k.eps2};
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+        cudaError_t el = launch_planned(plan, pr, reinterpret_cast<float4 *>(k.acc),
+                                        static_cast<float4 *>(scratch), dev->sm_count, cap);
+        if (el == cudaSuccess)
+            el = nbody::launch_euler(reinterpret_cast<float4 *>(const_cast<float *>(k.pm)),
+                                     reinterpret_cast<float4 *>(k.vel),
+                                     reinterpret_cast<const float4 *>(k.acc), ni, k.dt,
+                                     dev->sm_count, cap);
+        e = cudaStreamEndCapture(cap, &graph);
+        if (el != cudaSuccess) e = el;
+    }
+    cudaGraphExec_t exec = nullptr;
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+    if (graph != nullptr) cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+        if (scratch != nullptr) cudaFreeAsync(scratch, stream);
+        return cuda_fail(e);
+    }
+    g.key = k;
+    g.exec = exec;
+    g.scratch = scratch;
+    g.valid = true;
     return NBODY_OK;
 }
 
@@ -285,44 +440,61 @@ nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
         const nbody::ClusterVariant &cv = nbody::cluster_variant(v);
         cocc[v] = ctas_per_sm > 0 ? ctas_per_sm : nominal_occ(cv.i_per_thread, cv.warps * 32);
     }
-    return make_plan(n, sm_count, occ, cocc, opts, plan);
+    return make_plan(n, n, sm_count, occ, cocc, opts, plan);
 }
 
 nbody_status nbody_forces_ex(const float *pos_mass, int64_t n, float eps2, float *acc_pot,
                              const nbody_forces_opts *opts, cudaStream_t stream) {
     nbody_status st = check_forces(pos_mass, n, eps2, acc_pot);
     if (st != NBODY_OK || n == 0) return st;
+    const nbody::Problem pr = {pos_mass, pos_mass, static_cast<int>(n), static_cast<int>(n), eps2};
+    return run_forces(pr, opts, acc_pot, stream);
+}
+
+nbody_status nbody_forces_ts(const float *targets, int64_t nt, const float *sources, int64_t ns,
+                             float eps2, float *out, cudaStream_t stream) {
+    if (check_n(nt) != NBODY_OK || check_n(ns) != NBODY_OK) return NBODY_ERR_INVALID_ARG;
+    if (nt == 0) return NBODY_OK;
+    if (targets == nullptr || out == nullptr || (ns > 0 && sources == nullptr))
+        return NBODY_ERR_INVALID_ARG;
+    if (!std::isfinite(eps2) || !(eps2 >= FLT_MIN)) return NBODY_ERR_INVALID_ARG;
+    if (!aligned16(targets) || !aligned16(out) || (ns > 0 && !aligned16(sources)))
+        return NBODY_ERR_MISALIGNED;
+    if (overlap(out, targets, 16 * nt)) return NBODY_ERR_ALIAS;
+    if (ns > 0 && overlap2(out, 16 * nt, sources, 16 * ns)) return NBODY_ERR_ALIAS;
+    if (ns == 0) {   // no sources: every sum is empty
+        const cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(16 * nt), stream);
+        return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
+    }
+    const nbody::Problem pr = {targets, sources, static_cast<int>(nt), static_cast<int>(ns), eps2};
+    return run_forces(pr, nullptr, out, stream);
+}
+
+nbody_status nbody_simulate(float *pos_mass, float *vel, float *acc_pot, int64_t n, float eps2,
+                            float dt, int64_t steps, cudaStream_t stream) {
+    nbody_status st = check_forces(pos_mass, n, eps2, acc_pot);
+    if (st != NBODY_OK) return st;
+    if (steps < 0 || !std::isfinite(dt)) return NBODY_ERR_INVALID_ARG;
+    if (n == 0 || steps == 0) return NBODY_OK;
+    if (vel == nullptr) return NBODY_ERR_INVALID_ARG;
+    if (!aligned16(vel)) return NBODY_ERR_MISALIGNED;
+    if (overlap(vel, pos_mass, 16 * n) || overlap(vel, acc_pot, 16 * n)) return NBODY_ERR_ALIAS;
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != NBODY_OK) return st;
-    nbody_plan plan;
-    if ((st = make_plan(n, dev->sm_count, dev->tiled_occ, dev->cluster_occ, opts, &plan)) != NBODY_OK)
-        return st;
-
-    const int ni = static_cast<int>(n);
-    float4 *out = reinterpret_cast<float4 *>(acc_pot);
-    const int ntiles = static_cast<int>(ceil_div(n, plan.tile));
-    cudaError_t e;
-    if (plan.path == NBODY_PATH_CLUSTER) {
-        e = nbody::launch_cluster(plan.variant, pos_mass, ni, eps2, plan.num_iblocks, plan.cluster,
-                                  plan.tiles_per_split, ntiles, out, stream);
-        return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
-    }
-    if (plan.splits == 1) {
-        e = nbody::launch_tiled(plan.variant, pos_mass, ni, eps2, plan.num_iblocks, 1,
-                                plan.tiles_per_split, ntiles, out, stream);
-        return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
-    }
-    void *scratch = nullptr;
-    e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.scratch_bytes), dev->pool, stream);
+    int dev_id = 0;
+    cudaError_t e = cudaGetDevice(&dev_id);
     if (e != cudaSuccess) return cuda_fail(e);
-    float4 *part = static_cast<float4 *>(scratch);
-    e = nbody::launch_tiled(plan.variant, pos_mass, ni, eps2, plan.num_iblocks, plan.splits,
-                            plan.tiles_per_split, ntiles, part, stream);
-    if (e == cudaSuccess)
-        e = nbody::launch_reduce_splits(part, ni, plan.splits, out, dev->sm_count, stream);
-    const cudaError_t ef = cudaFreeAsync(scratch, stream);
-    if (e == cudaSuccess) e = ef;
-    return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
+    std::lock_guard<std::mutex> lock(g_sim_mu);
+    SimGraph &g = g_sim[dev_id];
+    const SimKey key = {pos_mass, vel, acc_pot, n, eps2, dt};
+    if (!(g.valid && g.key == key)) {
+        if (g.valid && (st = sim_release(g, stream)) != NBODY_OK) return st;
+        if ((st = sim_build(dev_id, dev, key, g, stream)) != NBODY_OK) return st;
+    }
+    for (int64_t s = 0; s < steps; ++s)
+        if ((e = cudaGraphLaunch(g.exec, stream)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaEventRecord(g.done, stream)) != cudaSuccess) return cuda_fail(e);
+    return NBODY_OK;
 }
 
 nbody_status nbody_forces(const float *pos_mass, int64_t n, float eps2, float *acc_pot,

@@ -6,6 +6,16 @@
 
 namespace nbody {
 
+// One force evaluation: every target against every source.  The all-pairs
+// call passes the same array as targets and sources.
+struct Problem {
+    const float *targets;   // nt records (x, y, z, w); w is not read
+    const float *sources;   // ns records (x, y, z, m)
+    int nt;
+    int ns;
+    float eps2;
+};
+
 // A compiled instantiation of the tiled force kernel.
 struct TiledVariant {
     int i_per_thread;   // K target bodies per thread (even: lanes of f32x2 pairs)
@@ -19,10 +29,9 @@ const TiledVariant &tiled_variant(int v);
 
 // Force kernel over grid = num_ib * splits CTAs; CTA b handles i-block
 // b % num_ib and source tiles [s * tps, min((s + 1) * tps, ntiles)) with
-// s = b / num_ib.  Writes out[s * n + i] (out = acc_pot when splits == 1).
-cudaError_t launch_tiled(int variant, const float *pos_mass, int n, float eps2, int num_ib,
-                         int splits, int tiles_per_split, int ntiles, float4 *out,
-                         cudaStream_t stream);
+// s = b / num_ib.  Writes out[s * nt + i] (out = the result when splits == 1).
+cudaError_t launch_tiled(int variant, const Problem &pr, int num_ib, int splits,
+                         int tiles_per_split, int ntiles, float4 *out, cudaStream_t stream);
 
 // A compiled instantiation of the small-N cluster kernel.
 struct ClusterVariant {
@@ -38,9 +47,8 @@ const ClusterVariant &cluster_variant(int v);
 // Cluster kernel over grid = num_ib * cluster CTAs in clusters of `cluster`;
 // cluster b handles targets [b * 32K, (b + 1) * 32K), its CTA of rank c the
 // source tiles [c * tpc, min((c + 1) * tpc, ntiles)).  Writes out[i] directly.
-cudaError_t launch_cluster(int variant, const float *pos_mass, int n, float eps2, int num_ib,
-                           int cluster, int tiles_per_cta, int ntiles, float4 *out,
-                           cudaStream_t stream);
+cudaError_t launch_cluster(int variant, const Problem &pr, int num_ib, int cluster,
+                           int tiles_per_cta, int ntiles, float4 *out, cudaStream_t stream);
 
 // out[i] = sum over s of part[s * n + i], in the order s = 0, 1, ..., compensated.
 cudaError_t launch_reduce_splits(const float4 *part, int n, int splits, float4 *out,

@@ -123,12 +123,13 @@ extern "C" nbody_status nbody_forces_noalloc(const float *pos_mass, int64_t n, f
     const int ni = static_cast<int>(n);
     const int ntiles = static_cast<int>((n + best.tile - 1) / best.tile);
     float4 *out = reinterpret_cast<float4 *>(acc_pot);
+    const nbody::Problem pr = {pos_mass, pos_mass, ni, ni, eps2};
     cudaError_t e;
     if (best.splits == 1) {
-        e = nbody::launch_tiled(best.variant, pos_mass, ni, eps2, best.num_iblocks, 1,
-                                best.tiles_per_split, ntiles, out, stream);
+        e = nbody::launch_tiled(best.variant, pr, best.num_iblocks, 1, best.tiles_per_split,
+                                ntiles, out, stream);
     } else {
-        e = nbody::launch_tiled(best.variant, pos_mass, ni, eps2, best.num_iblocks, best.splits,
+        e = nbody::launch_tiled(best.variant, pr, best.num_iblocks, best.splits,
                                 best.tiles_per_split, ntiles, dev->scratch, stream);
         if (e == cudaSuccess)
             e = nbody::launch_reduce_splits(dev->scratch, ni, best.splits, out, dev->sm_count,

@@ -91,6 +91,47 @@ nbody_status nbody_forces(const float *pos_mass, int64_t n, float eps2,
 nbody_status nbody_euler_step(float *pos_mass, float *vel, const float *acc_pot,
                               int64_t n, float dt, cudaStream_t stream);
 
+/*
+ * nbody_forces_ts -- target/source form: the acceleration and potential at
+ * each of nt targets from all ns sources, the same pair law and arithmetic
+ * as nbody_forces (which is the case targets == sources).  This is the
+ * near-field leaf interaction of hierarchical codes, which keep all-pairs for
+ * close cells (GPU Gems 3 ch.31 study page, section 6; Aizu slides No.30-34).
+ *
+ *   targets : device, nt records (x, y, z, w); w is not read.
+ *   sources : device, ns records (x, y, z, m).  May be the targets array.
+ *   out     : device, nt records (ax, ay, az, p); must overlap neither input.
+ *
+ * Every source counts, including one that sits exactly on a target (it adds
+ * 0 to a and -m/eps to p).  ns == 0 writes zeros; nt == 0 is a no-op.
+ * Errors: as nbody_forces.
+ */
+nbody_status nbody_forces_ts(const float *targets, int64_t nt, const float *sources, int64_t ns,
+                             float eps2, float *out, cudaStream_t stream);
+
+/*
+ * nbody_simulate -- `steps` explicit Euler steps of the self-gravitating
+ * system, device-resident: each step is nbody_forces(pos_mass -> acc_pot)
+ * followed by nbody_euler_step, exactly as the two calls would do it (same
+ * kernels, bit-identical results).  It replaces the host loop of the
+ * lecture's program (slide 13, the commented time loop) and of the Aizu host
+ * flow (No.10, upload / run / read back / integrate on the host).
+ *
+ *   pos_mass, vel : device, n records each; updated in place.
+ *   acc_pot       : device, n records; on return it holds (a, p) of the last
+ *                   step's starting positions.
+ *   steps         : >= 0 (0 is a no-op).
+ *
+ * One step is captured once into a CUDA graph and replayed `steps` times on
+ * `stream`.  The library keeps one such graph per device, keyed by the
+ * pointers, n, eps2 and dt; a call with other arguments rebuilds it (tens of
+ * microseconds).  Its split scratch comes from the library's pool and lives
+ * with the graph.  Do not call it inside a stream capture of your own.
+ * Errors: as nbody_forces and nbody_euler_step.
+ */
+nbody_status nbody_simulate(float *pos_mass, float *vel, float *acc_pot, int64_t n, float eps2,
+                            float dt, int64_t steps, cudaStream_t stream);
+
 /* Human-readable name of a status code; never NULL. */
 const char *nbody_status_string(nbody_status s);
 

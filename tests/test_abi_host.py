@@ -70,6 +70,47 @@ def test_forces_argument_checks(lib):
     assert _forces(lib, P + 144, 10, 1e-4, P) == 3
 
 
+def test_forces_ts_argument_checks(lib):
+    def call(t, nt, s, ns, eps2, out):
+        return lib.nbody_forces_ts(ctypes.c_void_p(t), nt, ctypes.c_void_p(s), ns,
+                                   ctypes.c_float(eps2), ctypes.c_void_p(out), None)
+    t, s, o = P, P + 4096, P + 8192
+    # every call below is rejected (or is a no-op) on the host
+    assert call(t, 0, s, 5, 1e-4, o) == 0                 # no targets: no-op
+    assert call(t, -1, s, 5, 1e-4, o) == 1
+    assert call(t, 5, s, -1, 1e-4, o) == 1
+    assert call(t, 5, s, 2 ** 31, 1e-4, o) == 1
+    assert call(0, 5, s, 5, 1e-4, o) == 1
+    assert call(t, 5, 0, 5, 1e-4, o) == 1                 # sources needed when ns > 0
+    assert call(t, 5, s, 5, 1e-4, 0) == 1
+    assert call(t, 5, s, 5, 0.0, o) == 1
+    assert call(t, 5, s, 5, float("nan"), o) == 1
+    assert call(t + 8, 5, s, 5, 1e-4, o) == 2
+    assert call(t, 5, s + 4, 5, 1e-4, o) == 2
+    assert call(t, 5, s, 5, 1e-4, o + 12) == 2
+    assert call(t, 5, s, 5, 1e-4, t + 64) == 3            # out overlaps the targets
+    assert call(t, 5, s, 300, 1e-4, s + 4000) == 3        # out overlaps the sources' tail
+    assert call(t, 2, s, 5, 1e-4, s - 16) == 3            # out's tail overlaps the sources
+
+
+def test_simulate_argument_checks(lib):
+    def call(pm, v, a, n, eps2, dt, steps):
+        return lib.nbody_simulate(ctypes.c_void_p(pm), ctypes.c_void_p(v), ctypes.c_void_p(a), n,
+                                  ctypes.c_float(eps2), ctypes.c_float(dt), steps, None)
+    a, b, c = P, P + 4096, P + 8192
+    # every call below is rejected (or is a no-op) on the host
+    assert call(a, b, c, 0, 1e-4, 1e-3, 5) == 0
+    assert call(a, b, c, 5, 1e-4, 1e-3, 0) == 0
+    assert call(a, b, c, 5, 1e-4, 1e-3, -1) == 1
+    assert call(a, b, c, 5, 1e-4, float("nan"), 3) == 1
+    assert call(a, b, c, 5, 0.0, 1e-3, 3) == 1
+    assert call(a, 0, c, 5, 1e-4, 1e-3, 3) == 1
+    assert call(a, b + 8, c, 5, 1e-4, 1e-3, 3) == 2
+    assert call(a, a + 32, c, 5, 1e-4, 1e-3, 3) == 3
+    assert call(a, b, a + 16, 5, 1e-4, 1e-3, 3) == 3
+    assert call(a, c + 16, c, 5, 1e-4, 1e-3, 3) == 3
+
+
 def test_euler_argument_checks(lib):
     def call(pm, v, a, n, dt):
         return lib.nbody_euler_step(ctypes.c_void_p(pm), ctypes.c_void_p(v), ctypes.c_void_p(a), n,

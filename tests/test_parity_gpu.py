@@ -292,3 +292,112 @@ def test_euler_large_bit_exact():
     pm_ref, v_ref = oracle.euler(w.pos_mass, w.vel, acc, w.dt)
     assert np.array_equal(pm.cpu().numpy(), pm_ref)
     assert np.array_equal(vel.cpu().numpy(), v_ref)
+
+
+# ------------------------------------------------------------ target/source form
+
+def _ts_bodies(nt, ns, seed):
+    st = W.Stream(seed)
+    t = np.zeros((nt, 4), np.float32)
+    t[:, :3] = st.uniform(3 * nt, -1.5, 1.5).reshape(nt, 3)
+    t[:, 3] = st.uniform(nt, 5.0, 9.0)             # never read
+    s = np.zeros((ns, 4), np.float32)
+    s[:, :3] = st.uniform(3 * ns, -1.0, 1.0).reshape(ns, 3)
+    s[:, 3] = st.uniform(ns, 0.5, 1.5)
+    return t, s
+
+
+@pytest.mark.parametrize("nt,ns", [(1, 1), (1, 1000), (1000, 1), (100, 5000), (5000, 100),
+                                   (3000, 20000), (20000, 3000), (77777, 1025), (1025, 77777)])
+def test_target_source_form(nt, ns):
+    t, s = _ts_bodies(nt, ns, nt * 7 + ns)
+    eps2 = np.float32(1e-3)
+    out = apg.nbody_forces_ts(torch.from_numpy(t).to(dev()), torch.from_numpy(s).to(dev()),
+                              float(eps2))
+    torch.cuda.synchronize()
+    assert_parity(out.cpu().numpy(), oracle.forces_ts(t, s, eps2))
+
+
+def test_target_source_golden_three_body():
+    """The worked three-body example through the target/source form: target 0
+    against the three bodies."""
+    pm = np.array([[0, 0, 0, 1.5], [3, 4, 0, 2], [1, 4, 8, 0.25]], np.float32)
+    tgt = torch.from_numpy(pm[:1].copy()).to(dev())
+    out = apg.nbody_forces_ts(tgt, torch.from_numpy(pm).to(dev()), 144.0).cpu().numpy()
+    exp = [6 / 2197 + 1 / 13500, 8 / 2197 + 1 / 3375, 2 / 3375, -2 / 13 - 1 / 60 - 1 / 8]
+    np.testing.assert_allclose(out[0].astype(np.float64), exp, rtol=2e-6)
+
+
+def test_target_source_no_sources_writes_zeros():
+    t = torch.full((37, 4), 3.0, device=dev())
+    out = torch.full_like(t, float("nan"))
+    apg.nbody_forces_ts(t, torch.empty((0, 4), device=dev()), 1e-4, out)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0
+
+
+@pytest.mark.parametrize("n", [1000, 30011])
+def test_target_source_equals_all_pairs_when_same_array(n):
+    w = W.clumps(n, seed=n)
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    a = apg.nbody_forces(pm, float(w.eps2))
+    b = apg.nbody_forces_ts(pm, pm, float(w.eps2))
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------ multi-step driver
+
+def _separate_steps(w, steps):
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    vel = torch.from_numpy(w.vel).to(dev())
+    acc = torch.empty_like(pm)
+    for _ in range(steps):
+        apg.nbody_forces(pm, float(w.eps2), acc)
+        apg.nbody_euler_step(pm, vel, acc, float(w.dt))
+    torch.cuda.synchronize()
+    return pm, vel, acc
+
+
+@pytest.mark.parametrize("name,steps", [("smallcube1024", 20), ("plummer65536", 10),
+                                        ("clumps200003", 2)])
+def test_simulate_is_the_separate_calls(name, steps):
+    w = W.named(name)
+    ref = _separate_steps(w, steps)
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    vel = torch.from_numpy(w.vel).to(dev())
+    acc = torch.empty_like(pm)
+    apg.nbody_simulate(pm, vel, acc, float(w.eps2), float(w.dt), steps)
+    torch.cuda.synchronize()
+    for got, exp in zip((pm, vel, acc), ref):
+        assert torch.equal(got, exp)
+
+
+def test_simulate_graph_cache_rebuilds():
+    """Alternate between two problems (the cached graph is rebuilt each time)
+    and repeat one (the cached graph is replayed): every result matches."""
+    wa, wb = W.small_cube(2048), W.plummer(20000, seed=3, eps=0.01)
+    bufs = {}
+    for w in (wa, wb):
+        pm = torch.from_numpy(w.pos_mass).to(dev())
+        bufs[w.name] = (w, pm, torch.from_numpy(w.vel).to(dev()), torch.empty_like(pm))
+    plan = [("smallcube2048", 3), ("plummer20000", 2), ("smallcube2048", 1), ("smallcube2048", 4)]
+    done = {"smallcube2048": 0, "plummer20000": 0}
+    for name, k in plan:
+        w, pm, vel, acc = bufs[name]
+        apg.nbody_simulate(pm, vel, acc, float(w.eps2), float(w.dt), k)
+        done[name] += k
+    torch.cuda.synchronize()
+    for name, (w, pm, vel, acc) in bufs.items():
+        ref = _separate_steps(w, done[name])
+        assert torch.equal(pm, ref[0]) and torch.equal(vel, ref[1]) and torch.equal(acc, ref[2])
+
+
+def test_simulate_zero_steps_is_a_noop():
+    w = W.small_cube(1024)
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    vel = torch.from_numpy(w.vel).to(dev())
+    acc = torch.zeros_like(pm)
+    apg.nbody_simulate(pm, vel, acc, float(w.eps2), float(w.dt), 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(pm.cpu().numpy(), w.pos_mass) and torch.count_nonzero(acc).item() == 0
