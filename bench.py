@@ -2,7 +2,7 @@
 Plummer bodies (the headline workload), timed with CUDA events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config NAME] [--no-cpu-baseline] [--no-e2e]
+                    [--config NAME] [--no-cpu-baseline] [--no-e2e] [--no-small-n]
 
 Prints one JSON line on rank 0.  `value` is interactions/s of the whole job
 (N^2 pairs per step and GPU) with inputs resident in HBM; `e2e` is the same
@@ -34,6 +34,16 @@ FP32_OPS_PER_PAIR = 13        # fp32 lane operations the pair law executes (a + 
 FP32_LANES_PER_SM_CLK = 128
 RECIPE_SM_MAX_MHZ = 2070.0    # fallback if no measured peaks file is present
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the force kernel at N = 2^20, from one ncu capture, keyed by a hash of the
+# kernel's source files: a changed kernel reports null until it is re-measured.
+KERNEL_SOURCES = ["all_pairs_gravitational_gb300/csrc/forces_tiled.cu",
+                  "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"]
+TRAFFIC_BY_SOURCE = {
+    "186a0bef5d143dde": {"bytes": 24.84e6 + 83.25e6,
+                         "profile": "profiles/forces_tiled_plummer1048576_dram.md"},
+}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -44,9 +54,65 @@ def parse():
     ap.add_argument("--config", default="plummer1048576")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-small-n", action="store_true",
+                    help="skip the small-N sweep (CUDA-graph-timed force calls, N = 1024..8192)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the CPU baseline sample")
     return ap.parse_args()
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def small_n_sweep(apg, W, device, sizes=(1024, 2048, 4096, 8192), reps=20):
+    """Force-call time for the small-N sweep, replayed from a CUDA graph so that
+    host launch overhead is excluded; plus nbody_simulate's per-step time."""
+    import torch
+    out = []
+    for n in sizes:
+        w = W.small_cube(n)
+        pm = torch.from_numpy(w.pos_mass).to(device)
+        acc = torch.empty_like(pm)
+        eps2 = float(w.eps2)
+        apg.nbody_forces(pm, eps2, acc)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                apg.nbody_forces(pm, eps2, acc)
+        g.replay()
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            b.synchronize()
+            t = a.elapsed_time(b) / reps
+            best = t if best is None else min(best, t)
+        vel = torch.zeros_like(pm)
+        steps = 100
+        apg.nbody_simulate(pm, vel, acc, eps2, float(w.dt), steps)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        apg.nbody_simulate(pm, vel, acc, eps2, float(w.dt), steps)
+        b.record()
+        b.synchronize()
+        plan = apg.nbody_plan_forces(n, torch.cuda.get_device_properties(device).multi_processor_count)
+        out.append({"n": n, "forces_us": round(best * 1e3, 2),
+                    "interactions_per_s": float(n) * n / (best / 1e3),
+                    "simulate_us_per_step": round(a.elapsed_time(b) * 1e3 / steps, 2),
+                    "path": "cluster" if plan["path"] == 2 else "tiled",
+                    "cluster": plan["cluster"], "splits": plan["splits"]})
+    return out
 
 
 def measured_peaks():
@@ -174,14 +240,20 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """The largest x over all ranks (the slowest rank's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_value(pairs_per_rank, step_ms, world):
+    """Interactions/s of the whole job: every rank's pairs over the slowest rank's step."""
+    return world * pairs_per_rank / (step_ms / 1e3)
 
 
 def run_reference(args):
@@ -290,7 +362,7 @@ def run_ours(args):
     euler_s = statistics.mean(euler_ms) / 1e3
     hbm = float(peaks.get("hbm_gbs", 6800.0))
 
-    value = world * pairs / (step_ms / 1e3)
+    value = whole_job_value(pairs, step_ms, world)
 
     e2e = None
     if not args.no_e2e:
@@ -299,6 +371,10 @@ def run_ours(args):
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = time_oracle(w, args.cpu_seconds)
+
+    sweep = None if args.no_small_n else small_n_sweep(apg, W, device)
+    src_hash = kernel_source_hash()
+    traffic = TRAFFIC_BY_SOURCE.get(src_hash) if w.name == "plummer1048576" else None
 
     sm_at_clock = clocks.get("sm_mhz")
     line = {
@@ -327,7 +403,9 @@ def run_ours(args):
             "peak": peak_pairs,
             "unit": "interactions/s",
             "frac": achieved / peak_pairs,
-            "traffic": None,
+            "traffic": traffic["bytes"] if traffic else None,
+            "traffic_source": (traffic["profile"] if traffic else
+                               f"not measured for kernel source {src_hash}"),
             "kernel": "forces_tiled_kernel (+ split reduction)",
             "peak_basis": (f"{props.multi_processor_count} SMs x {sm_max:.0f} MHz ({peaks_src}) x "
                            f"{FP32_LANES_PER_SM_CLK} fp32 lanes / {FP32_OPS_PER_PAIR} fp32 ops per pair"),
@@ -340,6 +418,7 @@ def run_ours(args):
                   "gbs": 80 * n / euler_s / 1e9, "hbm_peak_gbs": hbm,
                   "note": "inputs may be L2-resident at this size (84 MB < 129 MB L2)"},
         "cpu_baseline": cpu,
+        "small_n": sweep,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
