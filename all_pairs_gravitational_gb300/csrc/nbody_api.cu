@@ -90,6 +90,12 @@ nbody_status device_state(DeviceState **out) {
         }
         for (int v = 0; v < nbody::cluster_variant_count() && v < kMaxVariants; ++v) {
             const nbody::ClusterVariant &cv = nbody::cluster_variant(v);
+            if (cv.whole &&
+                (e = cudaFuncSetAttribute(cv.fn_pot, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(nbody::kWholeSmemMax))) != cudaSuccess)
+                return cuda_fail(e);
+            // register-limited residency (whole-range launches are further
+            // limited by their shared memory, see plan_cluster_variant)
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.cluster_occ[v], cv.fn_pot,
                                                               cv.warps * 32, 0);
             if (e != cudaSuccess) return cuda_fail(e);
@@ -111,6 +117,7 @@ nbody_status device_state(DeviceState **out) {
 // ---------------------------------------------------------------- planner
 
 constexpr int kDefaultTiledVariant = 0;
+constexpr int kDefaultClusterVariant = 0;
 constexpr int kMaxSplits = 1024;
 constexpr int64_t kMaxScratchBytes = int64_t(2) << 30;
 // Relative cost model (only ratios matter): pair rate of one SM, the fixed
@@ -173,7 +180,11 @@ void plan_tiled(int64_t nt, int64_t ns, int sm, int occ, int variant, int splits
 // CTAs (waves beyond the occupancy limit are counted), and an SM reaches its
 // full pair rate with kWarpsToSaturate resident warps.
 constexpr int kWarpsToSaturate = 16;
-
+// Cost of one CTA-wide barrier of the tiled cluster kernel, in source bodies.
+constexpr int kTileBarrierBodies = 32;
+// Shared memory of one SM available to resident CTAs (sm_103: 228 KB, 1 KB
+// reserved per CTA).
+constexpr int64_t kSmemPerSm = 228 * 1024;
 void plan_cluster_variant(int64_t nt, int64_t ns, int sm, int occ, int variant, nbody_plan *p,
                           double *t_out) {
     const nbody::ClusterVariant &v = nbody::cluster_variant(variant);
@@ -186,13 +197,23 @@ void plan_cluster_variant(int64_t nt, int64_t ns, int sm, int occ, int variant, 
     for (int64_t c = 1; c <= 8; c *= 2) {
         if (c > ntiles) break;
         const int64_t tpc = ceil_div(ntiles, c);
+        int64_t occ_c = occ > 0 ? occ : 1;
+        if (v.whole) {
+            const int64_t smem = static_cast<int64_t>(
+                nbody::whole_smem_bytes(v.i_per_thread, v.warps, static_cast<int>(tpc)));
+            if (smem > static_cast<int64_t>(nbody::kWholeSmemMax)) continue;
+            occ_c = std::min<int64_t>(occ_c, kSmemPerSm / (smem + 1024));
+            if (occ_c < 1) continue;
+        }
         const int64_t ctas = num_ib * c;
         const int64_t per_sm = ceil_div(ctas, sm);
-        const int64_t resident = std::min<int64_t>(per_sm, occ > 0 ? occ : 1);
+        const int64_t resident = std::min<int64_t>(per_sm, occ_c);
         const int64_t waves = ceil_div(per_sm, resident);
         const double rate = kPairsPerSmSecond *
                             std::min(1.0, static_cast<double>(resident * v.warps) / kWarpsToSaturate);
-        const double cta_pairs = static_cast<double>(tpc * v.tile + kItemOverheadBodies) * bi;
+        const int64_t barrier_bodies = v.whole ? kTileBarrierBodies : tpc * kTileBarrierBodies;
+        const double cta_pairs =
+            static_cast<double>(tpc * v.tile + kItemOverheadBodies + barrier_bodies) * bi;
         const double t = waves * resident * cta_pairs / rate + 0.2e-6 * (c > 1);
         if (t < best_t * (1.0 - 1e-3)) {
             best_t = t;
@@ -200,6 +221,10 @@ void plan_cluster_variant(int64_t nt, int64_t ns, int sm, int occ, int variant, 
             best_tpc = tpc;
             best_fill = static_cast<double>(ctas) / static_cast<double>(waves * resident * sm);
         }
+    }
+    if (!std::isfinite(best_t)) {   // no cluster size fits this variant's shared memory
+        *t_out = INFINITY;
+        return;
     }
     p->path = NBODY_PATH_CLUSTER;
     p->variant = variant;
@@ -242,9 +267,14 @@ nbody_status make_plan(int64_t nt, int64_t ns, int sm, const int *tiled_occ,
     }
     if (o.splits != 0) return NBODY_ERR_INVALID_ARG;   // the cluster path plans its own split
     if (o.variant >= nbody::cluster_variant_count()) return NBODY_ERR_INVALID_ARG;
+    // The cost model picks the cluster size well but ranks the kernel
+    // variants poorly; measured inside CUDA graphs on GB300, variant 0 is the
+    // fastest or within a few percent from 1024 to 6144 bodies, so automatic
+    // planning uses it and a forced variant is honoured.
+    const int only = o.variant >= 0 ? o.variant : kDefaultClusterVariant;
     double best = INFINITY;
     for (int v = 0; v < nbody::cluster_variant_count(); ++v) {
-        if (o.variant >= 0 && v != o.variant) continue;
+        if (v != only) continue;
         nbody_plan cand;
         double t;
         plan_cluster_variant(nt, ns, sm, cluster_occ[v], v, &cand, &t);
@@ -253,7 +283,8 @@ nbody_status make_plan(int64_t nt, int64_t ns, int sm, const int *tiled_occ,
             *p = cand;
         }
     }
-    return NBODY_OK;
+    // a forced whole-range variant whose range cannot fit shared memory
+    return std::isfinite(best) ? NBODY_OK : NBODY_ERR_INVALID_ARG;
 }
 
 // Launch a planned force evaluation; `scratch` holds plan.scratch_bytes when

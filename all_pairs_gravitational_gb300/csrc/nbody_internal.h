@@ -38,8 +38,16 @@ struct ClusterVariant {
     int i_per_thread;   // K targets per lane (even); the cluster's target block is 32 K
     int warps;          // W warps per CTA, each taking a slice of every source tile
     int tile;           // source bodies per shared-memory tile
+    bool whole;         // stages the CTA's whole source range at once (dynamic smem)
     const void *fn_pot;
 };
+
+// Dynamic shared memory a whole-range cluster launch needs.
+size_t whole_smem_bytes(int K, int W, int tiles_per_cta);
+
+// Largest dynamic shared memory a whole-range CTA may use (the sm_103 opt-in
+// limit is 227 KB per block).
+constexpr size_t kWholeSmemMax = 200 * 1024;
 
 int cluster_variant_count();
 const ClusterVariant &cluster_variant(int v);

@@ -401,3 +401,40 @@ def test_simulate_zero_steps_is_a_noop():
     apg.nbody_simulate(pm, vel, acc, float(w.eps2), float(w.dt), 0)
     torch.cuda.synchronize()
     assert np.array_equal(pm.cpu().numpy(), w.pos_mass) and torch.count_nonzero(acc).item() == 0
+
+
+# ------------------------------------------------------------ large arrays (64-bit offsets)
+
+@pytest.mark.slow
+def test_huge_source_array():
+    """2^26 + 5 sources (1 GiB): source offsets past 2^31 bytes, a ragged last
+    tile, hundreds of source splits; 300 targets checked against the oracle."""
+    ns, nt = 2 ** 26 + 5, 300
+    st = W.Stream(99)
+    s = np.empty((ns, 4), np.float32)
+    s[:, :3] = st.uniform(3 * ns, -1.0, 1.0).reshape(ns, 3)
+    s[:, 3] = np.float32(1.0 / ns)
+    t = np.zeros((nt, 4), np.float32)
+    t[:, :3] = st.uniform(3 * nt, -0.5, 0.5).reshape(nt, 3)
+    out = apg.nbody_forces_ts(torch.from_numpy(t).to(dev()), torch.from_numpy(s).to(dev()), 1e-4)
+    torch.cuda.synchronize()
+    assert_parity(out.cpu().numpy(), oracle.forces_ts(t, s, np.float32(1e-4)))
+
+
+@pytest.mark.slow
+def test_huge_target_array():
+    """2^26 targets (1 GiB in, 1 GiB out) against 77 sources: target and
+    output offsets past 2^31 bytes; sampled rows, the last ones included."""
+    nt, ns = 2 ** 26, 77
+    st = W.Stream(98)
+    t = np.empty((nt, 4), np.float32)
+    t[:, :3] = st.uniform(3 * nt, -2.0, 2.0).reshape(nt, 3)
+    t[:, 3] = 0.0
+    s = np.zeros((ns, 4), np.float32)
+    s[:, :3] = st.uniform(3 * ns, -1.0, 1.0).reshape(ns, 3)
+    s[:, 3] = st.uniform(ns, 0.5, 1.5)
+    out = apg.nbody_forces_ts(torch.from_numpy(t).to(dev()), torch.from_numpy(s).to(dev()), 1e-3)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([sample_rows(nt, 4000, 7), np.arange(nt - 1100, nt)]))
+    got = out[torch.from_numpy(rows).to(dev())].cpu().numpy()
+    assert_parity(got, oracle.forces_ts(t[rows], s, np.float32(1e-3)))
