@@ -17,6 +17,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnbody.so
 NBODY_PATH_AUTO = 0
 NBODY_PATH_TILED = 1
 NBODY_PATH_CLUSTER = 2
+NBODY_PRECISION_DEFAULT = 0
+NBODY_PRECISION_COMPENSATED = 1
 
 STATUS_NAMES = {
     0: "NBODY_OK", 1: "NBODY_ERR_INVALID_ARG", 2: "NBODY_ERR_MISALIGNED", 3: "NBODY_ERR_ALIAS",
@@ -33,7 +35,7 @@ EXPORTS = ["nbody_forces", "nbody_euler_step", "nbody_status_string", "nbody_las
 
 class nbody_forces_opts(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("variant", ctypes.c_int32),
-                ("splits", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("splits", ctypes.c_int32), ("precision", ctypes.c_int32)]
 
 
 class nbody_plan(ctypes.Structure):
@@ -128,8 +130,8 @@ def _stream_handle(device, stream):
     return ctypes.c_void_p(int(stream.cuda_stream))
 
 
-def _opts(path=NBODY_PATH_AUTO, variant=-1, splits=0):
-    return nbody_forces_opts(int(path), int(variant), int(splits), 0)
+def _opts(path=NBODY_PATH_AUTO, variant=-1, splits=0, precision=NBODY_PRECISION_DEFAULT):
+    return nbody_forces_opts(int(path), int(variant), int(splits), int(precision))
 
 
 def nbody_forces(pos_mass, eps2, acc_pot=None, stream=None):
@@ -138,7 +140,7 @@ def nbody_forces(pos_mass, eps2, acc_pot=None, stream=None):
 
 
 def nbody_forces_ex(pos_mass, eps2, acc_pot=None, path=NBODY_PATH_AUTO, variant=-1, splits=0,
-                    stream=None):
+                    precision=NBODY_PRECISION_DEFAULT, stream=None):
     import torch
     lib = load_library()
     _bodies(pos_mass, "pos_mass")
@@ -148,7 +150,7 @@ def nbody_forces_ex(pos_mass, eps2, acc_pot=None, path=NBODY_PATH_AUTO, variant=
     _bodies(acc_pot, "acc_pot", n)
     if acc_pot.device != pos_mass.device:
         raise ValueError("pos_mass and acc_pot must be on the same device")
-    opts = _opts(path, variant, splits)
+    opts = _opts(path, variant, splits, precision)
     with torch.cuda.device(pos_mass.device):
         st = lib.nbody_forces_ex(_ptr(pos_mass), n, ctypes.c_float(float(eps2)), _ptr(acc_pot),
                                  ctypes.byref(opts), _stream_handle(pos_mass.device, stream))
@@ -232,11 +234,12 @@ def nbody_simulate(pos_mass, vel, acc_pot, eps2, dt, steps, stream=None):
         raise NbodyError(st, "nbody_simulate")
 
 
-def nbody_plan_forces(n, sm_count, ctas_per_sm=0, path=NBODY_PATH_AUTO, variant=-1, splits=0):
+def nbody_plan_forces(n, sm_count, ctas_per_sm=0, path=NBODY_PATH_AUTO, variant=-1, splits=0,
+                      precision=NBODY_PRECISION_DEFAULT):
     """Host-only: the decomposition nbody_forces would launch (a dict)."""
     lib = load_library()
     plan = nbody_plan()
-    opts = _opts(path, variant, splits)
+    opts = _opts(path, variant, splits, precision)
     st = lib.nbody_plan_forces(int(n), int(sm_count), int(ctas_per_sm), ctypes.byref(opts),
                                ctypes.byref(plan))
     if st != 0:

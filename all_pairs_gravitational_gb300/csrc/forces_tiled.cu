@@ -112,6 +112,9 @@ struct Totals<KP, NT, true> {
 // MODE 0: one source per step of the unrolled loop; 1: software-pipelined
 // (rsqrt of source j+1 issued before source j is finished); 2: two sources
 // per step, their instructions interleaved in source order.
+// MODE 3: compensated -- the rsqrt is refined by one Newton step and every
+// acceleration term is added to a Kahan sum (29 fp32 lane-operations per pair
+// instead of 13), for systems whose bodies see extreme cancellation.
 template <int K, int NT, int P, int MINB, bool TSMEM, int U, int MODE, bool POT>
 __global__ void __launch_bounds__(NT, MINB)
 forces_tiled_kernel(const Problem pr, int num_ib, int tiles_per_split, int ntiles,
@@ -230,6 +233,42 @@ forces_tiled_kernel(const Problem pr, int num_ib, int tiles_per_split, int ntile
                         tot.fold(q, 1, ay[q]);
                         tot.fold(q, 2, az[q]);
                     }
+                }
+            }
+        } else if constexpr (MODE == 3) {
+            const f2 one = f2_pack(1.0f, 1.0f);
+            const f2 half = f2_pack(0.5f, 0.5f);
+#pragma unroll U
+            for (int jj = 0; jj < P; ++jj) {
+                const float4 a = s4[2 * jj];
+                const float4 b = s4[2 * jj + 1];
+                const f2 xj = f2_pack(a.x, a.y);
+                const f2 yj = f2_pack(a.z, a.w);
+                const f2 zj = f2_pack(b.x, b.y);
+                const f2 mj = f2_pack(b.z, b.w);
+#pragma unroll
+                for (int q = 0; q < KP; ++q) {
+                    const f2 dx = f2_sub(xj, xi[q]);
+                    const f2 dy = f2_sub(yj, yi[q]);
+                    const f2 dz = f2_sub(zj, zi[q]);
+                    f2 d2 = f2_fma(dx, dx, e2);
+                    d2 = f2_fma(dy, dy, d2);
+                    d2 = f2_fma(dz, dz, d2);
+                    float d2a, d2b;
+                    f2_unpack(d2, d2a, d2b);
+                    const f2 r0 = f2_pack(rsqrt_hw(d2a), rsqrt_hw(d2b));
+                    // Newton: r = r0 + (r0 / 2) (1 - d2 r0^2)
+                    const f2 h = f2_mul(d2, r0);
+                    const f2 res = f2_fma(f2_sub(0ull, h), r0, one);
+                    const f2 inv = f2_fma(f2_mul(half, r0), res, r0);
+                    const f2 tm = f2_mul(mj, inv);
+                    const f2 inv2 = f2_mul(inv, inv);
+                    const f2 sc = f2_mul(tm, inv2);
+                    f2 tx = f2_mul(sc, dx), ty = f2_mul(sc, dy), tz = f2_mul(sc, dz);
+                    tot.fold(q, 0, tx);
+                    tot.fold(q, 1, ty);
+                    tot.fold(q, 2, tz);
+                    if (POT) pp[q] = f2_add(pp[q], tm);
                 }
             }
         } else if constexpr (MODE == 2) {
@@ -366,7 +405,8 @@ __global__ void reduce_splits_kernel(const float4 *__restrict__ part, int n, int
 // loop MODE.  Variant 0 is the default: the fastest on GB300 from N = 2^18
 // to 2^20 (2.50e12 pairs/s at N = 2^20; packed FMA with three fresh
 // operands tops out near 90 % of the pipe, and this reaches about 89 % of
-// that).  The others stay selectable for tuning and tests.
+// that).  Variant 8 is the compensated kernel that precision = 1 selects.
+// The others stay selectable for tuning and tests.
 #define NBODY_TILED_LIST(X)                                 \
     X(4, 256, 128, 2, true, 4, 2)   /* 0: default */         \
     X(4, 256, 128, 2, false, 8, 0)  /* 1 */                  \
@@ -375,7 +415,8 @@ __global__ void reduce_splits_kernel(const float4 *__restrict__ part, int n, int
     X(8, 128, 128, 3, false, 8, 0)  /* 4 */                  \
     X(4, 256, 128, 3, true, 8, 0)   /* 5 */                  \
     X(4, 256, 128, 2, false, 8, 1)  /* 6 */                  \
-    X(2, 256, 128, 4, false, 4, 2)  /* 7 */
+    X(2, 256, 128, 4, false, 4, 2)  /* 7 */                  \
+    X(4, 256, 128, 2, false, 4, 3)  /* 8: compensated (precision 1) */
 
 #define NBODY_TILED_ENTRY(K, NT, P, MINB, TS, U, MODE) \
     {K, NT, P, reinterpret_cast<const void *>(&forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, true>)},

@@ -118,6 +118,7 @@ nbody_status device_state(DeviceState **out) {
 
 constexpr int kDefaultTiledVariant = 0;
 constexpr int kDefaultClusterVariant = 0;
+constexpr int kCompensatedTiledVariant = 8;
 constexpr int kMaxSplits = 1024;
 constexpr int64_t kMaxScratchBytes = int64_t(2) << 30;
 // Relative cost model (only ratios matter): pair rate of one SM, the fixed
@@ -255,6 +256,13 @@ nbody_status make_plan(int64_t nt, int64_t ns, int sm, const int *tiled_occ,
     if (opts != nullptr) o = *opts;
     if (o.path < NBODY_PATH_AUTO || o.path > NBODY_PATH_CLUSTER || o.splits < 0)
         return NBODY_ERR_INVALID_ARG;
+    if (o.precision < 0 || o.precision > 1) return NBODY_ERR_INVALID_ARG;
+    if (o.precision == 1) {   // compensated: the tiled path's compensated kernel
+        if (o.path == NBODY_PATH_CLUSTER || (o.variant >= 0 && o.variant != kCompensatedTiledVariant))
+            return NBODY_ERR_INVALID_ARG;
+        o.path = NBODY_PATH_TILED;
+        o.variant = kCompensatedTiledVariant;
+    }
     int path = o.path;
     if (path == NBODY_PATH_AUTO)
         path = (nt <= kClusterMaxN && ns <= kClusterMaxN) ? NBODY_PATH_CLUSTER : NBODY_PATH_TILED;

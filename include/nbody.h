@@ -152,8 +152,20 @@ typedef struct nbody_forces_opts {
     int32_t path;       /* NBODY_PATH_* */
     int32_t variant;    /* kernel variant of the path; -1 = library default */
     int32_t splits;     /* tiled path: j-splits S (0 = planner's choice, 1 = none) */
-    int32_t reserved;
+    int32_t precision;  /* NBODY_PRECISION_* */
 } nbody_forces_opts;
+
+enum {
+    /* fp32 pair terms, fp32 partial sums folded into Kahan totals every 32
+     * sources (acceleration) or 1024 (potential): the default. */
+    NBODY_PRECISION_DEFAULT = 0,
+    /* fp32 pair terms with a Newton-refined rsqrt, and every acceleration term
+     * added to a Kahan sum: for bodies whose sum cancels heavily (near
+     * neighbours far stronger than the total).  About 2.2x the time; tiled
+     * path only.  The double-double arithmetic of the Aizu slides (No.21-22)
+     * is the model for compensated sums of fp32 terms. */
+    NBODY_PRECISION_COMPENSATED = 1
+};
 
 /* The decomposition nbody_forces would launch; host-only, needs no GPU. */
 typedef struct nbody_plan {

@@ -438,3 +438,27 @@ def test_huge_target_array():
     rows = np.unique(np.concatenate([sample_rows(nt, 4000, 7), np.arange(nt - 1100, nt)]))
     got = out[torch.from_numpy(rows).to(dev())].cpu().numpy()
     assert_parity(got, oracle.forces_ts(t[rows], s, np.float32(1e-3)))
+
+
+# ------------------------------------------------------------ compensated precision
+
+def test_compensated_precision_on_the_ill_conditioned_disk():
+    """Body 1888 of the disk workload has near neighbours 380x |a_i|
+    (condition number 1244): the compensated kernel cuts its error well
+    below the default kernel's."""
+    w = W.named("disk4096")
+    ref = oracle.forces(w.pos_mass, w.eps2)
+    base = errors(gpu_forces(w.pos_mass, w.eps2), ref, potential=False)
+    comp = errors(gpu_forces(w.pos_mass, w.eps2, precision=apg.NBODY_PRECISION_COMPENSATED), ref,
+                  potential=False)
+    assert comp["body_a"] <= 3e-5 and comp["body_a"] < 0.6 * base["body_a"], (base, comp)
+    assert comp["l2_a"] <= base["l2_a"]
+
+
+@pytest.mark.parametrize("name", ["cube16384", "clumps200003"])
+def test_compensated_precision_parity(name):
+    w = W.named(name)
+    got = gpu_forces(w.pos_mass, w.eps2, precision=apg.NBODY_PRECISION_COMPENSATED)
+    rows = np.arange(w.n) if w.n <= 20000 else sample_rows(w.n, 1500, 4)
+    e = assert_parity(got, oracle.forces(w.pos_mass, w.eps2, rows=rows), rows)
+    assert e["l2_a"] <= 1e-6 and e["l2_p"] <= 1e-6, e
