@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-small-n", action="store_true",
                     help="skip the small-N sweep (CUDA-graph-timed force calls, N = 1024..8192)")
+    ap.add_argument("--probe", choices=["euler"], default=None,
+                    help="run one kernel probe alone and print its result (for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the CPU baseline sample")
     return ap.parse_args()
@@ -113,6 +115,30 @@ def small_n_sweep(apg, W, device, sizes=(1024, 2048, 4096, 8192), reps=20):
                     "path": "cluster" if plan["path"] == 2 else "tiled",
                     "cluster": plan["cluster"], "splits": plan["splits"]})
     return out
+
+
+def euler_hbm_probe(apg, device, n=1 << 26, reps=5):
+    """The Euler kernel at a size far beyond L2 (80 B per body, 5.4 GB per
+    step at n = 2^26), L2 flushed before each timed launch: achieved HBM GB/s."""
+    import torch
+    pm = torch.rand((n, 4), device=device)
+    vel = torch.rand((n, 4), device=device)
+    acc = torch.rand((n, 4), device=device)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)
+    apg.nbody_euler_step(pm, vel, acc, 1e-6)
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        apg.nbody_euler_step(pm, vel, acc, 1e-6)
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.median(ts)
+    del pm, vel, acc, flush
+    torch.cuda.empty_cache()
+    return {"n": n, "ms": ms, "bytes": 80 * n, "gbs": 80 * n / (ms / 1e3) / 1e9}
 
 
 def measured_peaks():
@@ -373,6 +399,7 @@ def run_ours(args):
         cpu = time_oracle(w, args.cpu_seconds)
 
     sweep = None if args.no_small_n else small_n_sweep(apg, W, device)
+    euler_hbm = None if args.no_small_n else euler_hbm_probe(apg, device)
     src_hash = kernel_source_hash()
     traffic = TRAFFIC_BY_SOURCE.get(src_hash) if w.name == "plummer1048576" else None
 
@@ -416,7 +443,10 @@ def run_ours(args):
         },
         "euler": {"ms": statistics.mean(euler_ms), "bytes": 80 * n,
                   "gbs": 80 * n / euler_s / 1e9, "hbm_peak_gbs": hbm,
-                  "note": "inputs may be L2-resident at this size (84 MB < 129 MB L2)"},
+                  "note": "in-step figure; the 84 MB may be L2-resident at this size",
+                  "hbm_probe": (dict(euler_hbm, hbm_peak_gbs=hbm, frac=euler_hbm["gbs"] / hbm,
+                                     bound="hbm", peak_source=peaks_src)
+                                if euler_hbm else None)},
         "cpu_baseline": cpu,
         "small_n": sweep,
         "e2e": e2e,
@@ -470,9 +500,25 @@ def run_e2e(apg, w, device, steps, world):
             "h2d_bytes_per_step": 32 * n, "d2h_bytes_per_step": 48 * n, "ms_per_step": ms}
 
 
+def run_probe(args):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import all_pairs_gravitational_gb300 as apg
+    torch.cuda.set_device(0)
+    peaks, src = measured_peaks()
+    r = euler_hbm_probe(apg, torch.device("cuda", 0))
+    r.update(probe="euler_kernel", hbm_peak_gbs=float(peaks.get("hbm_gbs", 6800.0)), peak_source=src)
+    r["frac"] = r["gbs"] / r["hbm_peak_gbs"]
+    print(json.dumps(r), flush=True)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.probe:
+        run_probe(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
