@@ -8,32 +8,30 @@
 // several threads below about 4096 bodies and merges the partial
 // accelerations).  Here a cluster of C CTAs shares one block of BI = 32 K
 // targets; CTA c takes source tiles [c T, c T + T) and warp w of it takes
-// the w-th slice of every tile, so C * W pieces of the source range run in
+// the w-th slice of them, so C * W pieces of the source range run in
 // parallel, for N * BI / (C * W) pairs each.
 //
+// Two ways to feed the warps:
+//   * tiled (forces_cluster_kernel): 128-body tiles through a 3-stage cp.async
+//     ring, warp w taking the w-th slice of every tile;
+//   * whole range (forces_cluster_whole_kernel): the CTA's entire range staged
+//     into dynamic shared memory at once, one barrier, warp w taking the
+//     w-th contiguous slice.
+//
 // Reduction, deterministic and without atomics or global scratch:
-//   1. each warp folds its fp32 partials into Kahan totals (as in the tiled
-//      kernel) and writes them to shared memory;
+//   1. each warp folds its fp32 partials into Kahan totals and writes them to
+//      shared memory;
 //   2. the CTA adds its W warp partials in the order w = 0 .. W-1;
 //   3. after a cluster barrier, CTA c adds slice c of the targets over the C
 //      CTAs' shared memory, rank 0 .. C-1, and stores the result;
 //   4. a second cluster barrier keeps every CTA's shared memory alive until
 //      the other CTAs have read it.
-// Tiles are staged exactly as in forces_tiled.cu (cp.async, duplicated
-// layout, zero-filled tail); the pair arithmetic is the same.
 #include <algorithm>
 
 #include "nbody_device.cuh"
 #include "nbody_internal.h"
 
 namespace nbody {
-
-namespace {
-
-constexpr int kStages = 3;
-constexpr int kClusterTile = 128;   // source tile of the cluster path (both kernels)
-
-}  // namespace
 
 // Dynamic shared memory of the whole-range kernel: the staged range and the
 // per-warp partials.
@@ -42,6 +40,10 @@ size_t whole_smem_bytes(int K, int W, int tiles_per_cta) {
 }
 
 namespace {
+
+constexpr int kStages = 3;
+constexpr int kClusterTile = 128;   // source tile of the cluster path (both kernels)
+constexpr int kFoldJ = 32;          // sources between folds of a warp's partials
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -71,27 +73,109 @@ __device__ __forceinline__ float4 ld_dsmem_f4(const void *local, uint32_t rank) 
     return v;
 }
 
-template <int NT, int P>
-__device__ __forceinline__ void stage_tile(float *sbuf, const float *src_bodies, int ns, int tile) {
-    static_assert((8 * P) % NT == 0, "tile copies must divide evenly among threads");
-    const uint32_t sbase = smem_u32(sbuf);
-    const int64_t j0 = static_cast<int64_t>(tile) * P;
-#pragma unroll
-    for (int r = 0; r < (8 * P) / NT; ++r) {
-        const int idx = r * NT + static_cast<int>(threadIdx.x);
-        const int64_t j = j0 + (idx >> 3);
-        const int comp = (idx >> 1) & 3;
-        const bool ok = j < ns;
-        const float *src = src_bodies + (ok ? j * 4 + comp : 0);
-        cp_async_4(sbase + 4u * static_cast<uint32_t>(idx), src, ok ? 4 : 0);
-    }
+__device__ __forceinline__ void kahan4(float4 &h, float4 &c, const float4 &v) {
+    kahan1(h.x, c.x, v.x);
+    kahan1(h.y, c.y, v.y);
+    kahan1(h.z, c.z, v.z);
+    kahan1(h.w, c.w, v.w);
 }
 
-__device__ __forceinline__ void kahan1(float &hi, float &lo, float x) {
-    const float y = __fsub_rn(x, lo);
-    const float t = __fadd_rn(hi, y);
-    lo = __fsub_rn(__fsub_rn(t, hi), y);
-    hi = t;
+// One warp's accumulators for K targets per lane, KP = K/2 f32x2 pairs.
+template <int KP>
+struct WarpAcc {
+    f2 ax[KP], ay[KP], az[KP], pp[KP];   // fp32 partials since the last fold
+    f2 hx[KP], hy[KP], hz[KP], hp[KP];   // Kahan totals ...
+    f2 lx[KP], ly[KP], lz[KP], lp[KP];   // ... and corrections
+
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int q = 0; q < KP; ++q) {
+            ax[q] = ay[q] = az[q] = pp[q] = 0ull;
+            hx[q] = hy[q] = hz[q] = hp[q] = 0ull;
+            lx[q] = ly[q] = lz[q] = lp[q] = 0ull;
+        }
+    }
+
+    // Sources [j_begin, j_end) of a duplicated shared-memory run.
+    template <bool POT>
+    __device__ __forceinline__ void run(const float4 *s4, int j_begin, int j_end, const f2 (&xi)[KP],
+                                        const f2 (&yi)[KP], const f2 (&zi)[KP], f2 e2) {
+#pragma unroll 4
+        for (int jj = j_begin; jj < j_end; ++jj) {
+            const Src sj = load_src(s4, jj);
+#pragma unroll
+            for (int q = 0; q < KP; ++q) {
+                const Geom g = pair_geom(sj, xi[q], yi[q], zi[q], e2);
+                const f2 tm = pair_accumulate(g, sj.m, ax[q], ay[q], az[q]);
+                if (POT) pp[q] = f2_add(pp[q], tm);
+            }
+        }
+    }
+
+    __device__ __forceinline__ void fold_acc() {
+#pragma unroll
+        for (int q = 0; q < KP; ++q) {
+            f2_kahan_fold(hx[q], lx[q], ax[q]);
+            f2_kahan_fold(hy[q], ly[q], ay[q]);
+            f2_kahan_fold(hz[q], lz[q], az[q]);
+        }
+    }
+
+    __device__ __forceinline__ void fold_pot() {
+#pragma unroll
+        for (int q = 0; q < KP; ++q) f2_kahan_fold(hp[q], lp[q], pp[q]);
+    }
+};
+
+// Steps 1-4 of the reduction: warp partials -> CTA partial -> cluster sum ->
+// out[ib * BI + slot] for this CTA's slice of the target block.
+template <int K, int W, bool POT>
+__device__ __forceinline__ void reduce_and_store(WarpAcc<K / 2> &acc, float4 (*red)[32 * K],
+                                                 int ib, int nt, float4 *__restrict__ out) {
+    constexpr int KP = K / 2;
+    constexpr int BI = 32 * K;
+    constexpr int NT = W * 32;
+    const int tid = static_cast<int>(threadIdx.x);
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    // 1. warp partials to shared memory: slot k*32 + lane is target ib*BI + slot
+#pragma unroll
+    for (int q = 0; q < KP; ++q) {
+        float x0, x1, y0, y1, z0, z1, p0 = 0.f, p1 = 0.f;
+        f2_unpack(f2_sub(acc.hx[q], acc.lx[q]), x0, x1);
+        f2_unpack(f2_sub(acc.hy[q], acc.ly[q]), y0, y1);
+        f2_unpack(f2_sub(acc.hz[q], acc.lz[q]), z0, z1);
+        if (POT) f2_unpack(f2_sub(acc.hp[q], acc.lp[q]), p0, p1);
+        red[warp][(2 * q) * 32 + lane] = make_float4(x0, y0, z0, p0);
+        red[warp][(2 * q + 1) * 32 + lane] = make_float4(x1, y1, z1, p1);
+    }
+    __syncthreads();
+    // 2. CTA partial over warps w = 0 .. W-1, in place in red[0]
+    for (int slot = tid; slot < BI; slot += NT) {
+        float4 h = red[0][slot];
+        float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 1; w < W; ++w) kahan4(h, c, red[w][slot]);
+        red[0][slot] = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y),
+                                   __fsub_rn(h.z, c.z), __fsub_rn(h.w, c.w));
+    }
+    // 3. cluster partial over ranks 0 .. C-1 for this CTA's slice of targets
+    cluster_sync();
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t csize = cluster_nctarank();
+    const int per = BI / static_cast<int>(csize);
+    for (int t = tid; t < per; t += NT) {
+        const int slot = static_cast<int>(crank) * per + t;
+        float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 c = h;
+        for (uint32_t r = 0; r < csize; ++r) kahan4(h, c, ld_dsmem_f4(&red[0][slot], r));
+        const int64_t i = static_cast<int64_t>(ib) * BI + slot;
+        if (i < nt)
+            out[i] = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y), __fsub_rn(h.z, c.z),
+                                 -__fsub_rn(h.w, c.w));
+    }
+    // 4. keep this CTA's shared memory alive until every rank has read it
+    cluster_sync();
 }
 
 template <int K, int W, int P, bool POT>
@@ -104,45 +188,22 @@ forces_cluster_kernel(const Problem pr, int tiles_per_cta, int ntiles,
     constexpr int BI = 32 * K;          // targets per cluster
     constexpr int JW = P / W;           // sources per warp per tile
     constexpr int FOLD_P = 8;           // tiles between folds of the potential
-    static_assert(P % W == 0 && JW <= 32, "tile must split evenly, <= 32 sources per warp");
+    static_assert(P % W == 0 && JW <= kFoldJ, "tile must split evenly, <= 32 sources per warp");
 
     __shared__ __align__(16) float sdup[kStages][P * 8];
     __shared__ __align__(16) float4 red[W][BI];
 
-    const int tid = static_cast<int>(threadIdx.x);
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const uint32_t crank = cluster_ctarank();
-    const uint32_t csize = cluster_nctarank();
-    const int ib = static_cast<int>(blockIdx.x / csize);
-    const int t_begin = static_cast<int>(crank) * tiles_per_cta;
+    const int warp = static_cast<int>(threadIdx.x) >> 5;
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+    const int ib = static_cast<int>(blockIdx.x / cluster_nctarank());
+    const int t_begin = static_cast<int>(cluster_ctarank()) * tiles_per_cta;
     const int t_end = min(t_begin + tiles_per_cta, ntiles);
-    const int64_t ibase = static_cast<int64_t>(ib) * BI + lane;
-    const float4 *tg4 = reinterpret_cast<const float4 *>(pr.targets);
-    const int n = pr.nt;   // targets
 
     f2 xi[KP], yi[KP], zi[KP];
-#pragma unroll
-    for (int q = 0; q < KP; ++q) {
-        const int64_t i0 = min(ibase + (2 * q) * 32, static_cast<int64_t>(n) - 1);
-        const int64_t i1 = min(ibase + (2 * q + 1) * 32, static_cast<int64_t>(n) - 1);
-        const float4 b0 = __ldg(tg4 + i0);
-        const float4 b1 = __ldg(tg4 + i1);
-        xi[q] = f2_pack(b0.x, b1.x);
-        yi[q] = f2_pack(b0.y, b1.y);
-        zi[q] = f2_pack(b0.z, b1.z);
-    }
+    load_targets<KP>(pr.targets, pr.nt, static_cast<int64_t>(ib) * BI + lane, 32, xi, yi, zi);
     const f2 e2 = f2_pack(pr.eps2, pr.eps2);
-
-    f2 ax[KP], ay[KP], az[KP], pp[KP];
-    f2 hx[KP], hy[KP], hz[KP], hp[KP];
-    f2 lx[KP], ly[KP], lz[KP], lp[KP];
-#pragma unroll
-    for (int q = 0; q < KP; ++q) {
-        ax[q] = ay[q] = az[q] = pp[q] = 0ull;
-        hx[q] = hy[q] = hz[q] = hp[q] = 0ull;
-        lx[q] = ly[q] = lz[q] = lp[q] = 0ull;
-    }
+    WarpAcc<KP> acc;
+    acc.init();
 
     if (t_begin < t_end) stage_tile<NT, P>(sdup[0], pr.sources, pr.ns, t_begin);
     cp_async_commit();
@@ -160,108 +221,19 @@ forces_cluster_kernel(const Problem pr, int tiles_per_cta, int ntiles,
             if (t + 2 < t_end) stage_tile<NT, P>(sdup[s2], pr.sources, pr.ns, t + 2);
             cp_async_commit();
         }
-        const float4 *s4 = reinterpret_cast<const float4 *>(sdup[stage]) + 2 * (warp * JW);
-#pragma unroll 4
-        for (int jj = 0; jj < JW; ++jj) {
-            const float4 a = s4[2 * jj];
-            const float4 b = s4[2 * jj + 1];
-            const f2 xj = f2_pack(a.x, a.y);
-            const f2 yj = f2_pack(a.z, a.w);
-            const f2 zj = f2_pack(b.x, b.y);
-            const f2 mj = f2_pack(b.z, b.w);
-#pragma unroll
-            for (int q = 0; q < KP; ++q) {
-                const f2 dx = f2_sub(xj, xi[q]);
-                const f2 dy = f2_sub(yj, yi[q]);
-                const f2 dz = f2_sub(zj, zi[q]);
-                f2 d2 = f2_fma(dx, dx, e2);
-                d2 = f2_fma(dy, dy, d2);
-                d2 = f2_fma(dz, dz, d2);
-                float d2a, d2b;
-                f2_unpack(d2, d2a, d2b);
-                const f2 inv = f2_pack(rsqrt_hw(d2a), rsqrt_hw(d2b));
-                const f2 tm = f2_mul(mj, inv);
-                const f2 inv2 = f2_mul(inv, inv);
-                const f2 s = f2_mul(tm, inv2);
-                ax[q] = f2_fma(s, dx, ax[q]);
-                ay[q] = f2_fma(s, dy, ay[q]);
-                az[q] = f2_fma(s, dz, az[q]);
-                if (POT) pp[q] = f2_add(pp[q], tm);
-            }
-        }
-        // acceleration: fold after every warp slice (<= 32 sources, see
-        // forces_tiled.cu); potential: every FOLD_P tiles
-#pragma unroll
-        for (int q = 0; q < KP; ++q) {
-            f2_kahan_fold(hx[q], lx[q], ax[q]);
-            f2_kahan_fold(hy[q], ly[q], ay[q]);
-            f2_kahan_fold(hz[q], lz[q], az[q]);
-        }
-        if (POT && ((k + 1) % FOLD_P == 0 || t + 1 == t_end)) {
-#pragma unroll
-            for (int q = 0; q < KP; ++q) f2_kahan_fold(hp[q], lp[q], pp[q]);
-        }
+        const float4 *s4 = reinterpret_cast<const float4 *>(sdup[stage]);
+        acc.template run<POT>(s4, warp * JW, (warp + 1) * JW, xi, yi, zi, e2);
+        acc.fold_acc();                                   // every warp slice (<= 32 sources)
+        if (POT && ((k + 1) % FOLD_P == 0 || t + 1 == t_end)) acc.fold_pot();
         stage = (stage + 1 == kStages) ? 0 : stage + 1;
     }
     cp_async_wait<0>();
-
-    // 1. warp partials to shared memory: slot k*32 + lane is target ib*BI + slot
-#pragma unroll
-    for (int q = 0; q < KP; ++q) {
-        float x0, x1, y0, y1, z0, z1, p0 = 0.f, p1 = 0.f;
-        f2_unpack(f2_sub(hx[q], lx[q]), x0, x1);
-        f2_unpack(f2_sub(hy[q], ly[q]), y0, y1);
-        f2_unpack(f2_sub(hz[q], lz[q]), z0, z1);
-        if (POT) f2_unpack(f2_sub(hp[q], lp[q]), p0, p1);
-        red[warp][(2 * q) * 32 + lane] = make_float4(x0, y0, z0, p0);
-        red[warp][(2 * q + 1) * 32 + lane] = make_float4(x1, y1, z1, p1);
-    }
-    __syncthreads();
-
-    // 2. CTA partial over warps w = 0 .. W-1, in place in red[0]
-    for (int slot = tid; slot < BI; slot += NT) {
-        float4 h = red[0][slot];
-        float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 1; w < W; ++w) {
-            const float4 v = red[w][slot];
-            kahan1(h.x, c.x, v.x);
-            kahan1(h.y, c.y, v.y);
-            kahan1(h.z, c.z, v.z);
-            kahan1(h.w, c.w, v.w);
-        }
-        red[0][slot] = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y),
-                                   __fsub_rn(h.z, c.z), __fsub_rn(h.w, c.w));
-    }
-
-    // 3. cluster partial over ranks 0 .. C-1 for this CTA's slice of targets
-    cluster_sync();
-    const int per = BI / static_cast<int>(csize);
-    for (int t = tid; t < per; t += NT) {
-        const int slot = static_cast<int>(crank) * per + t;
-        float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 c = h;
-        for (uint32_t r = 0; r < csize; ++r) {
-            const float4 v = ld_dsmem_f4(&red[0][slot], r);
-            kahan1(h.x, c.x, v.x);
-            kahan1(h.y, c.y, v.y);
-            kahan1(h.z, c.z, v.z);
-            kahan1(h.w, c.w, v.w);
-        }
-        const int64_t i = static_cast<int64_t>(ib) * BI + slot;
-        if (i < n)
-            out[i] = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y), __fsub_rn(h.z, c.z),
-                                 -__fsub_rn(h.w, c.w));
-    }
-    // 4. keep this CTA's shared memory alive until every rank has read it
-    cluster_sync();
+    reduce_and_store<K, W, POT>(acc, red, ib, pr.nt, out);
 }
 
-// Whole-range variant: the CTA's entire source range (tiles_per_cta * 128
-// bodies, at most a few thousand for the N this path serves) is staged into
-// dynamic shared memory at once, with one barrier, and each warp then runs
-// over a contiguous slice of it.  This removes the per-tile barriers, which
-// at small N leave each warp only 16-32 sources between barriers.
+// Whole-range variant: see the file header.  The CTA's range is
+// tiles_per_cta * 128 bodies (a few thousand at most for the N this path
+// serves), zero-filled past ns.
 template <int K, int W, bool POT>
 __global__ void __launch_bounds__(W * 32)
 forces_cluster_whole_kernel(const Problem pr, int tiles_per_cta, float4 *__restrict__ out) {
@@ -269,58 +241,25 @@ forces_cluster_whole_kernel(const Problem pr, int tiles_per_cta, float4 *__restr
     constexpr int KP = K / 2;
     constexpr int NT = W * 32;
     constexpr int BI = 32 * K;
-    constexpr int FOLDJ = 32;
 
     extern __shared__ __align__(16) float4 dyn[];
     const int jc = tiles_per_cta * kClusterTile;          // sources staged by this CTA
     float *sdup = reinterpret_cast<float *>(dyn);          // jc bodies x 8 floats
     float4 (*red)[BI] = reinterpret_cast<float4 (*)[BI]>(dyn + 2 * jc);
 
-    const int tid = static_cast<int>(threadIdx.x);
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const uint32_t crank = cluster_ctarank();
-    const uint32_t csize = cluster_nctarank();
-    const int ib = static_cast<int>(blockIdx.x / csize);
-    const int64_t j0 = static_cast<int64_t>(crank) * jc;
-    const int64_t ibase = static_cast<int64_t>(ib) * BI + lane;
-    const float4 *tg4 = reinterpret_cast<const float4 *>(pr.targets);
-    const int n = pr.nt;
+    const int warp = static_cast<int>(threadIdx.x) >> 5;
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+    const int ib = static_cast<int>(blockIdx.x / cluster_nctarank());
+    const int64_t j0 = static_cast<int64_t>(cluster_ctarank()) * jc;
 
-    // stage the whole range: bodies past ns are written as zeros
-    {
-        const uint32_t sbase = smem_u32(sdup);
-        for (int idx = tid; idx < 8 * jc; idx += NT) {
-            const int64_t j = j0 + (idx >> 3);
-            const int comp = (idx >> 1) & 3;
-            const bool ok = j < pr.ns;
-            const float *src = pr.sources + (ok ? j * 4 + comp : 0);
-            cp_async_4(sbase + 4u * static_cast<uint32_t>(idx), src, ok ? 4 : 0);
-        }
-        cp_async_commit();
-    }
+    stage_sources<NT>(sdup, pr.sources, pr.ns, j0, jc);
+    cp_async_commit();
 
     f2 xi[KP], yi[KP], zi[KP];
-#pragma unroll
-    for (int q = 0; q < KP; ++q) {
-        const int64_t i0 = min(ibase + (2 * q) * 32, static_cast<int64_t>(n) - 1);
-        const int64_t i1 = min(ibase + (2 * q + 1) * 32, static_cast<int64_t>(n) - 1);
-        const float4 b0 = __ldg(tg4 + i0);
-        const float4 b1 = __ldg(tg4 + i1);
-        xi[q] = f2_pack(b0.x, b1.x);
-        yi[q] = f2_pack(b0.y, b1.y);
-        zi[q] = f2_pack(b0.z, b1.z);
-    }
+    load_targets<KP>(pr.targets, pr.nt, static_cast<int64_t>(ib) * BI + lane, 32, xi, yi, zi);
     const f2 e2 = f2_pack(pr.eps2, pr.eps2);
-    f2 ax[KP], ay[KP], az[KP], pp[KP];
-    f2 hx[KP], hy[KP], hz[KP], hp[KP];
-    f2 lx[KP], ly[KP], lz[KP], lp[KP];
-#pragma unroll
-    for (int q = 0; q < KP; ++q) {
-        ax[q] = ay[q] = az[q] = pp[q] = 0ull;
-        hx[q] = hy[q] = hz[q] = hp[q] = 0ull;
-        lx[q] = ly[q] = lz[q] = lp[q] = 0ull;
-    }
+    WarpAcc<KP> acc;
+    acc.init();
 
     cp_async_wait<0>();
     __syncthreads();
@@ -328,131 +267,17 @@ forces_cluster_whole_kernel(const Problem pr, int tiles_per_cta, float4 *__restr
     // warp slice: jw sources (jc / W, a multiple of 16), folded every 32
     const int jw = jc / W;
     const float4 *s4 = reinterpret_cast<const float4 *>(sdup) + 2 * (warp * jw);
-    for (int jb = 0; jb < jw; jb += FOLDJ) {
-        const int je = min(jb + FOLDJ, jw);
-#pragma unroll 4
-        for (int jj = jb; jj < je; ++jj) {
-            const float4 a = s4[2 * jj];
-            const float4 b = s4[2 * jj + 1];
-            const f2 xj = f2_pack(a.x, a.y);
-            const f2 yj = f2_pack(a.z, a.w);
-            const f2 zj = f2_pack(b.x, b.y);
-            const f2 mj = f2_pack(b.z, b.w);
-#pragma unroll
-            for (int q = 0; q < KP; ++q) {
-                const f2 dx = f2_sub(xj, xi[q]);
-                const f2 dy = f2_sub(yj, yi[q]);
-                const f2 dz = f2_sub(zj, zi[q]);
-                f2 d2 = f2_fma(dx, dx, e2);
-                d2 = f2_fma(dy, dy, d2);
-                d2 = f2_fma(dz, dz, d2);
-                float d2a, d2b;
-                f2_unpack(d2, d2a, d2b);
-                const f2 inv = f2_pack(rsqrt_hw(d2a), rsqrt_hw(d2b));
-                const f2 tm = f2_mul(mj, inv);
-                const f2 inv2 = f2_mul(inv, inv);
-                const f2 sc = f2_mul(tm, inv2);
-                ax[q] = f2_fma(sc, dx, ax[q]);
-                ay[q] = f2_fma(sc, dy, ay[q]);
-                az[q] = f2_fma(sc, dz, az[q]);
-                if (POT) pp[q] = f2_add(pp[q], tm);
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < KP; ++q) {
-            f2_kahan_fold(hx[q], lx[q], ax[q]);
-            f2_kahan_fold(hy[q], ly[q], ay[q]);
-            f2_kahan_fold(hz[q], lz[q], az[q]);
-            if (POT) f2_kahan_fold(hp[q], lp[q], pp[q]);
-        }
+    for (int jb = 0; jb < jw; jb += kFoldJ) {
+        acc.template run<POT>(s4, jb, min(jb + kFoldJ, jw), xi, yi, zi, e2);
+        acc.fold_acc();
+        if (POT) acc.fold_pot();
     }
-
-    // reductions as in forces_cluster_kernel: warps, then cluster ranks
-#pragma unroll
-    for (int q = 0; q < KP; ++q) {
-        float x0, x1, y0, y1, z0, z1, p0 = 0.f, p1 = 0.f;
-        f2_unpack(f2_sub(hx[q], lx[q]), x0, x1);
-        f2_unpack(f2_sub(hy[q], ly[q]), y0, y1);
-        f2_unpack(f2_sub(hz[q], lz[q]), z0, z1);
-        if (POT) f2_unpack(f2_sub(hp[q], lp[q]), p0, p1);
-        red[warp][(2 * q) * 32 + lane] = make_float4(x0, y0, z0, p0);
-        red[warp][(2 * q + 1) * 32 + lane] = make_float4(x1, y1, z1, p1);
-    }
-    __syncthreads();
-    for (int slot = tid; slot < BI; slot += NT) {
-        float4 h = red[0][slot];
-        float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 1; w < W; ++w) {
-            const float4 v = red[w][slot];
-            kahan1(h.x, c.x, v.x);
-            kahan1(h.y, c.y, v.y);
-            kahan1(h.z, c.z, v.z);
-            kahan1(h.w, c.w, v.w);
-        }
-        red[0][slot] = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y),
-                                   __fsub_rn(h.z, c.z), __fsub_rn(h.w, c.w));
-    }
-    cluster_sync();
-    const int per = BI / static_cast<int>(csize);
-    for (int t = tid; t < per; t += NT) {
-        const int slot = static_cast<int>(crank) * per + t;
-        float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 c = h;
-        for (uint32_t r = 0; r < csize; ++r) {
-            const float4 v = ld_dsmem_f4(&red[0][slot], r);
-            kahan1(h.x, c.x, v.x);
-            kahan1(h.y, c.y, v.y);
-            kahan1(h.z, c.z, v.z);
-            kahan1(h.w, c.w, v.w);
-        }
-        const int64_t i = static_cast<int64_t>(ib) * BI + slot;
-        if (i < n)
-            out[i] = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y), __fsub_rn(h.z, c.z),
-                                 -__fsub_rn(h.w, c.w));
-    }
-    cluster_sync();
+    reduce_and_store<K, W, POT>(acc, red, ib, pr.nt, out);
 }
-
-template <int K, int W>
-cudaError_t launch_whole(const Problem &pr, int num_ib, int cluster, int tpc, float4 *out,
-                         cudaStream_t stream) {
-    const size_t smem = whole_smem_bytes(K, W, tpc);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(num_ib) * static_cast<unsigned>(cluster), 1, 1);
-    cfg.blockDim = dim3(W * 32, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, true>, pr, tpc, out);
-}
-
-#define NBODY_CLUSTER(K, W, P) {K, W, P, false, reinterpret_cast<const void *>(&forces_cluster_kernel<K, W, P, true>)}
-#define NBODY_CLUSTER_WHOLE(K, W) {K, W, kClusterTile, true, reinterpret_cast<const void *>(&forces_cluster_whole_kernel<K, W, true>)}
-
-const ClusterVariant kVariants[] = {
-    NBODY_CLUSTER(2, 4, 128),   // 0
-    NBODY_CLUSTER(4, 4, 128),   // 1
-    NBODY_CLUSTER(2, 8, 128),   // 2
-    NBODY_CLUSTER(4, 8, 128),   // 3
-    NBODY_CLUSTER_WHOLE(2, 4),  // 4: whole source range staged at once
-    NBODY_CLUSTER_WHOLE(4, 4),  // 5
-    NBODY_CLUSTER_WHOLE(2, 8),  // 6
-    NBODY_CLUSTER_WHOLE(4, 8),  // 7
-};
-
-#undef NBODY_CLUSTER
-#undef NBODY_CLUSTER_WHOLE
 
 template <int K, int W, int P>
-cudaError_t launch_variant(const Problem &pr, int num_ib, int cluster, int tpc, int ntiles,
-                           float4 *out, cudaStream_t stream) {
+cudaError_t launch_tiled_cluster(const Problem &pr, int num_ib, int cluster, int tpc, int ntiles,
+                                 float4 *out, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_ib) * static_cast<unsigned>(cluster), 1, 1);
     cfg.blockDim = dim3(W * 32, 1, 1);
@@ -468,6 +293,41 @@ cudaError_t launch_variant(const Problem &pr, int num_ib, int cluster, int tpc, 
     return cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true>, pr, tpc, ntiles, out);
 }
 
+template <int K, int W>
+cudaError_t launch_whole(const Problem &pr, int num_ib, int cluster, int tpc, float4 *out,
+                         cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_ib) * static_cast<unsigned>(cluster), 1, 1);
+    cfg.blockDim = dim3(W * 32, 1, 1);
+    cfg.dynamicSmemBytes = whole_smem_bytes(K, W, tpc);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, true>, pr, tpc, out);
+}
+
+#define NBODY_CLUSTER(K, W, P) {K, W, P, false, reinterpret_cast<const void *>(&forces_cluster_kernel<K, W, P, true>)}
+#define NBODY_CLUSTER_WHOLE(K, W) {K, W, kClusterTile, true, reinterpret_cast<const void *>(&forces_cluster_whole_kernel<K, W, true>)}
+
+const ClusterVariant kVariants[] = {
+    NBODY_CLUSTER(2, 4, 128),   // 0: default
+    NBODY_CLUSTER(4, 4, 128),   // 1
+    NBODY_CLUSTER(2, 8, 128),   // 2
+    NBODY_CLUSTER(4, 8, 128),   // 3
+    NBODY_CLUSTER_WHOLE(2, 4),  // 4: whole source range staged at once
+    NBODY_CLUSTER_WHOLE(4, 4),  // 5
+    NBODY_CLUSTER_WHOLE(2, 8),  // 6
+    NBODY_CLUSTER_WHOLE(4, 8),  // 7
+};
+
+#undef NBODY_CLUSTER
+#undef NBODY_CLUSTER_WHOLE
+
 }  // namespace
 
 int cluster_variant_count() { return static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0])); }
@@ -477,10 +337,10 @@ const ClusterVariant &cluster_variant(int v) { return kVariants[v]; }
 cudaError_t launch_cluster(int variant, const Problem &pr, int num_ib, int cluster,
                            int tiles_per_cta, int ntiles, float4 *out, cudaStream_t stream) {
     switch (variant) {
-        case 0: return launch_variant<2, 4, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
-        case 1: return launch_variant<4, 4, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
-        case 2: return launch_variant<2, 8, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
-        case 3: return launch_variant<4, 8, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        case 0: return launch_tiled_cluster<2, 4, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        case 1: return launch_tiled_cluster<4, 4, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        case 2: return launch_tiled_cluster<2, 8, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
+        case 3: return launch_tiled_cluster<4, 8, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
         case 4: return launch_whole<2, 4>(pr, num_ib, cluster, tiles_per_cta, out, stream);
         case 5: return launch_whole<4, 4>(pr, num_ib, cluster, tiles_per_cta, out, stream);
         case 6: return launch_whole<2, 8>(pr, num_ib, cluster, tiles_per_cta, out, stream);

@@ -118,7 +118,7 @@ nbody_status device_state(DeviceState **out) {
 
 constexpr int kDefaultTiledVariant = 0;
 constexpr int kDefaultClusterVariant = 0;
-constexpr int kCompensatedTiledVariant = 8;
+constexpr int kCompensatedTiledVariant = 7;
 constexpr int kMaxSplits = 1024;
 constexpr int64_t kMaxScratchBytes = int64_t(2) << 30;
 // Relative cost model (only ratios matter): pair rate of one SM, the fixed

@@ -192,7 +192,7 @@ def test_auto_path_choice():
 def test_compensated_precision_plans_the_compensated_kernel():
     for n in (1, 1000, 4096, 1048576):
         plan = apg.nbody_plan_forces(n, 152, precision=apg.NBODY_PRECISION_COMPENSATED)
-        assert plan["path"] == apg.NBODY_PATH_TILED and plan["variant"] == 8
+        assert plan["path"] == apg.NBODY_PATH_TILED and plan["variant"] == 7
         _covers(plan, n)
     with pytest.raises(apg.NbodyError):
         apg.nbody_plan_forces(1000, 152, path=apg.NBODY_PATH_CLUSTER,
