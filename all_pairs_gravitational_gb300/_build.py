@@ -7,6 +7,8 @@ library with the CUDA runtime linked statically.  ptxas resource usage
 from __future__ import annotations
 
 import concurrent.futures as cf
+import contextlib
+import fcntl
 import glob
 import os
 import shutil
@@ -46,11 +48,29 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
+@contextlib.contextmanager
+def _build_lock():
+    """One build at a time: ranks launched together share the build folder."""
+    os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as f:
+        fcntl.flock(f, fcntl.LOCK_EX)
+        try:
+            yield
+        finally:
+            fcntl.flock(f, fcntl.LOCK_UN)
+
+
 def build_library(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
+    with _build_lock():
+        if not force and up_to_date():      # another process built it meanwhile
+            return LIB
+        return _build(verbose)
+
+
+def _build(verbose: bool) -> str:
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")

@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-small-n", action="store_true",
                     help="skip the small-N sweep (CUDA-graph-timed force calls, N = 1024..8192)")
-    ap.add_argument("--probe", choices=["euler"], default=None,
+    ap.add_argument("--probe", choices=["euler", "configs"], default=None,
                     help="run one kernel probe alone and print its result (for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the CPU baseline sample")
@@ -82,23 +82,7 @@ def small_n_sweep(apg, W, device, sizes=(1024, 2048, 4096, 8192), reps=20):
         pm = torch.from_numpy(w.pos_mass).to(device)
         acc = torch.empty_like(pm)
         eps2 = float(w.eps2)
-        apg.nbody_forces(pm, eps2, acc)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(reps):
-                apg.nbody_forces(pm, eps2, acc)
-        g.replay()
-        torch.cuda.synchronize()
-        best = None
-        for _ in range(5):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            g.replay()
-            b.record()
-            b.synchronize()
-            t = a.elapsed_time(b) / reps
-            best = t if best is None else min(best, t)
+        best = graph_time_ms(lambda: apg.nbody_forces(pm, eps2, acc), reps)
         vel = torch.zeros_like(pm)
         steps = 100
         apg.nbody_simulate(pm, vel, acc, eps2, float(w.dt), steps)
@@ -500,18 +484,89 @@ def run_e2e(apg, w, device, steps, world):
             "h2d_bytes_per_step": 32 * n, "d2h_bytes_per_step": 48 * n, "ms_per_step": ms}
 
 
+def graph_time_ms(fn, reps):
+    """Per-call time of fn replayed `reps` times from one CUDA graph (best of 5)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        b.synchronize()
+        t = a.elapsed_time(b) / reps
+        best = t if best is None else min(best, t)
+    return best
+
+
+def configs_probe(apg, W, device):
+    """Every measured workload: the force call alone (replayed from a CUDA
+    graph, so host launch overhead is excluded), one nbody_simulate step, and
+    the fraction of the fp32-pipe peak."""
+    import torch
+    props = torch.cuda.get_device_properties(device)
+    peaks, _ = measured_peaks()
+    peak = props.multi_processor_count * float(peaks.get("sm_max_mhz", RECIPE_SM_MAX_MHZ)) * 1e6 * \
+        FP32_LANES_PER_SM_CLK / FP32_OPS_PER_PAIR
+    out = []
+    for name in W.CONFIG_NAMES + [f"smallcube{n}" for n in W.SMALL_SWEEP]:
+        w = W.named(name)
+        n = w.n
+        pm = torch.from_numpy(w.pos_mass).to(device)
+        vel = torch.from_numpy(w.vel).to(device)
+        acc = torch.empty_like(pm)
+        eps2, dt = float(w.eps2), float(w.dt)
+        reps = max(1, min(50, int(2e10 / (float(n) * n))))
+        ms = graph_time_ms(lambda: apg.nbody_forces(pm, eps2, acc), reps)
+        steps = max(1, min(100, int(1e11 / (float(n) * n))))
+        apg.nbody_simulate(pm, vel, acc, eps2, dt, steps)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        apg.nbody_simulate(pm, vel, acc, eps2, dt, steps)
+        b.record()
+        b.synchronize()
+        step_ms = a.elapsed_time(b) / steps
+        plan = apg.nbody_plan_forces(n, props.multi_processor_count)
+        rate = float(n) * n / (ms / 1e3)
+        cpu = time_oracle(w, 1.5)
+        out.append({"workload": name, "n": n, "forces_ms": ms, "interactions_per_s": rate,
+                    "gflops_20": rate * FLOPS_PER_PAIR / 1e9, "frac_fp32_peak": rate / peak,
+                    "simulate_step_ms": step_ms,
+                    "path": "cluster" if plan["path"] == 2 else "tiled",
+                    "splits": plan["splits"],
+                    "cpu_oracle_interactions_per_s": cpu["value"], "cpu_cores": cpu["cores"]})
+        del pm, vel, acc
+    return out
+
+
 def run_probe(args):
     import torch
 
     import __graft_entry__
     __graft_entry__.build()
     import all_pairs_gravitational_gb300 as apg
+    from all_pairs_gravitational_gb300 import workloads as W
     torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
     peaks, src = measured_peaks()
-    r = euler_hbm_probe(apg, torch.device("cuda", 0))
-    r.update(probe="euler_kernel", hbm_peak_gbs=float(peaks.get("hbm_gbs", 6800.0)), peak_source=src)
-    r["frac"] = r["gbs"] / r["hbm_peak_gbs"]
-    print(json.dumps(r), flush=True)
+    if args.probe == "euler":
+        r = euler_hbm_probe(apg, device)
+        r.update(probe="euler_kernel", hbm_peak_gbs=float(peaks.get("hbm_gbs", 6800.0)),
+                 peak_source=src)
+        r["frac"] = r["gbs"] / r["hbm_peak_gbs"]
+        print(json.dumps(r), flush=True)
+    else:
+        for r in configs_probe(apg, W, device):
+            print(json.dumps(r), flush=True)
 
 
 def main():
