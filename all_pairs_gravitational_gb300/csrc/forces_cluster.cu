@@ -18,6 +18,10 @@
 //     into dynamic shared memory at once, one barrier, warp w taking the
 //     w-th contiguous slice.
 //
+// Optionally (nbody_simulate) the kernel also applies the Euler step to each
+// target as it stores its result, writing the new position to a second
+// buffer, so that a small-N time step is one launch instead of two.
+//
 // Reduction, deterministic and without atomics or global scratch:
 //   1. each warp folds its fp32 partials into Kahan totals and writes them to
 //      shared memory;
@@ -129,9 +133,10 @@ struct WarpAcc {
 
 // Steps 1-4 of the reduction: warp partials -> CTA partial -> cluster sum ->
 // out[ib * BI + slot] for this CTA's slice of the target block.
-template <int K, int W, bool POT>
+template <int K, int W, bool POT, bool EULER>
 __device__ __forceinline__ void reduce_and_store(WarpAcc<K / 2> &acc, float4 (*red)[32 * K],
-                                                 int ib, int nt, float4 *__restrict__ out) {
+                                                 int ib, const Problem &pr,
+                                                 float4 *__restrict__ out, const EulerFuse &eu) {
     constexpr int KP = K / 2;
     constexpr int BI = 32 * K;
     constexpr int NT = W * 32;
@@ -170,18 +175,32 @@ __device__ __forceinline__ void reduce_and_store(WarpAcc<K / 2> &acc, float4 (*r
         float4 c = h;
         for (uint32_t r = 0; r < csize; ++r) kahan4(h, c, ld_dsmem_f4(&red[0][slot], r));
         const int64_t i = static_cast<int64_t>(ib) * BI + slot;
-        if (i < nt)
-            out[i] = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y), __fsub_rn(h.z, c.z),
-                                 -__fsub_rn(h.w, c.w));
+        if (i < pr.nt) {
+            const float4 a = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y),
+                                         __fsub_rn(h.z, c.z), -__fsub_rn(h.w, c.w));
+            out[i] = a;
+            if (EULER) {   // the step of euler.cu, on this body, positions first
+                float4 x = __ldg(reinterpret_cast<const float4 *>(pr.targets) + i);
+                float4 v = eu.vel[i];
+                x.x = __fadd_rn(x.x, __fmul_rn(eu.dt, v.x));
+                x.y = __fadd_rn(x.y, __fmul_rn(eu.dt, v.y));
+                x.z = __fadd_rn(x.z, __fmul_rn(eu.dt, v.z));
+                v.x = __fadd_rn(v.x, __fmul_rn(eu.dt, a.x));
+                v.y = __fadd_rn(v.y, __fmul_rn(eu.dt, a.y));
+                v.z = __fadd_rn(v.z, __fmul_rn(eu.dt, a.z));
+                eu.pos_out[i] = x;
+                eu.vel[i] = v;
+            }
+        }
     }
     // 4. keep this CTA's shared memory alive until every rank has read it
     cluster_sync();
 }
 
-template <int K, int W, int P, bool POT>
+template <int K, int W, int P, bool POT, bool EULER>
 __global__ void __launch_bounds__(W * 32)
 forces_cluster_kernel(const Problem pr, int tiles_per_cta, int ntiles,
-                      float4 *__restrict__ out) {
+                      float4 *__restrict__ out, const EulerFuse eu) {
     static_assert(K % 2 == 0, "targets are processed in f32x2 pairs");
     constexpr int KP = K / 2;
     constexpr int NT = W * 32;
@@ -228,15 +247,16 @@ forces_cluster_kernel(const Problem pr, int tiles_per_cta, int ntiles,
         stage = (stage + 1 == kStages) ? 0 : stage + 1;
     }
     cp_async_wait<0>();
-    reduce_and_store<K, W, POT>(acc, red, ib, pr.nt, out);
+    reduce_and_store<K, W, POT, EULER>(acc, red, ib, pr, out, eu);
 }
 
 // Whole-range variant: see the file header.  The CTA's range is
 // tiles_per_cta * 128 bodies (a few thousand at most for the N this path
 // serves), zero-filled past ns.
-template <int K, int W, bool POT>
+template <int K, int W, bool POT, bool EULER>
 __global__ void __launch_bounds__(W * 32)
-forces_cluster_whole_kernel(const Problem pr, int tiles_per_cta, float4 *__restrict__ out) {
+forces_cluster_whole_kernel(const Problem pr, int tiles_per_cta, float4 *__restrict__ out,
+                            const EulerFuse eu) {
     static_assert(K % 2 == 0, "targets are processed in f32x2 pairs");
     constexpr int KP = K / 2;
     constexpr int NT = W * 32;
@@ -272,12 +292,12 @@ forces_cluster_whole_kernel(const Problem pr, int tiles_per_cta, float4 *__restr
         acc.fold_acc();
         if (POT) acc.fold_pot();
     }
-    reduce_and_store<K, W, POT>(acc, red, ib, pr.nt, out);
+    reduce_and_store<K, W, POT, EULER>(acc, red, ib, pr, out, eu);
 }
 
 template <int K, int W, int P>
 cudaError_t launch_tiled_cluster(const Problem &pr, int num_ib, int cluster, int tpc, int ntiles,
-                                 float4 *out, cudaStream_t stream) {
+                                 float4 *out, cudaStream_t stream, const EulerFuse *eu) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_ib) * static_cast<unsigned>(cluster), 1, 1);
     cfg.blockDim = dim3(W * 32, 1, 1);
@@ -290,12 +310,16 @@ cudaError_t launch_tiled_cluster(const Problem &pr, int num_ib, int cluster, int
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true>, pr, tpc, ntiles, out);
+    if (eu != nullptr)
+        return cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true, true>, pr, tpc, ntiles,
+                                  out, *eu);
+    return cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true, false>, pr, tpc, ntiles,
+                              out, EulerFuse{nullptr, nullptr, 0.f});
 }
 
 template <int K, int W>
 cudaError_t launch_whole(const Problem &pr, int num_ib, int cluster, int tpc, float4 *out,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const EulerFuse *eu) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_ib) * static_cast<unsigned>(cluster), 1, 1);
     cfg.blockDim = dim3(W * 32, 1, 1);
@@ -308,11 +332,15 @@ cudaError_t launch_whole(const Problem &pr, int num_ib, int cluster, int tpc, fl
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, true>, pr, tpc, out);
+    if (eu != nullptr)
+        return cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, true, true>, pr, tpc, out,
+                                  *eu);
+    return cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, true, false>, pr, tpc, out,
+                              EulerFuse{nullptr, nullptr, 0.f});
 }
 
-#define NBODY_CLUSTER(K, W, P) {K, W, P, false, reinterpret_cast<const void *>(&forces_cluster_kernel<K, W, P, true>)}
-#define NBODY_CLUSTER_WHOLE(K, W) {K, W, kClusterTile, true, reinterpret_cast<const void *>(&forces_cluster_whole_kernel<K, W, true>)}
+#define NBODY_CLUSTER(K, W, P) {K, W, P, false, reinterpret_cast<const void *>(&forces_cluster_kernel<K, W, P, true, false>)}
+#define NBODY_CLUSTER_WHOLE(K, W) {K, W, kClusterTile, true, reinterpret_cast<const void *>(&forces_cluster_whole_kernel<K, W, true, false>)}
 
 const ClusterVariant kVariants[] = {
     NBODY_CLUSTER(2, 4, 128),   // 0: default
@@ -335,16 +363,18 @@ int cluster_variant_count() { return static_cast<int>(sizeof(kVariants) / sizeof
 const ClusterVariant &cluster_variant(int v) { return kVariants[v]; }
 
 cudaError_t launch_cluster(int variant, const Problem &pr, int num_ib, int cluster,
-                           int tiles_per_cta, int ntiles, float4 *out, cudaStream_t stream) {
+                           int tiles_per_cta, int ntiles, float4 *out, cudaStream_t stream,
+                           const EulerFuse *eu) {
+    const int tpc = tiles_per_cta;
     switch (variant) {
-        case 0: return launch_tiled_cluster<2, 4, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
-        case 1: return launch_tiled_cluster<4, 4, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
-        case 2: return launch_tiled_cluster<2, 8, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
-        case 3: return launch_tiled_cluster<4, 8, 128>(pr, num_ib, cluster, tiles_per_cta, ntiles, out, stream);
-        case 4: return launch_whole<2, 4>(pr, num_ib, cluster, tiles_per_cta, out, stream);
-        case 5: return launch_whole<4, 4>(pr, num_ib, cluster, tiles_per_cta, out, stream);
-        case 6: return launch_whole<2, 8>(pr, num_ib, cluster, tiles_per_cta, out, stream);
-        case 7: return launch_whole<4, 8>(pr, num_ib, cluster, tiles_per_cta, out, stream);
+        case 0: return launch_tiled_cluster<2, 4, 128>(pr, num_ib, cluster, tpc, ntiles, out, stream, eu);
+        case 1: return launch_tiled_cluster<4, 4, 128>(pr, num_ib, cluster, tpc, ntiles, out, stream, eu);
+        case 2: return launch_tiled_cluster<2, 8, 128>(pr, num_ib, cluster, tpc, ntiles, out, stream, eu);
+        case 3: return launch_tiled_cluster<4, 8, 128>(pr, num_ib, cluster, tpc, ntiles, out, stream, eu);
+        case 4: return launch_whole<2, 4>(pr, num_ib, cluster, tpc, out, stream, eu);
+        case 5: return launch_whole<4, 4>(pr, num_ib, cluster, tpc, out, stream, eu);
+        case 6: return launch_whole<2, 8>(pr, num_ib, cluster, tpc, out, stream, eu);
+        case 7: return launch_whole<4, 8>(pr, num_ib, cluster, tpc, out, stream, eu);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -344,7 +344,10 @@ nbody_status run_forces(const nbody::Problem &pr, const nbody_forces_opts *opts,
 // One step (forces, then Euler) is captured once into a CUDA graph on an
 // internal stream and replayed `steps` times on the caller's stream, so a
 // step costs one graph launch instead of two or three kernel launches from
-// the host.  One graph per device is cached, keyed by every argument but the
+// the host.  On the cluster path (small N) a second graph holds two steps
+// whose Euler update is fused into the force kernel, the positions going
+// from pos_mass to a library-owned second buffer and back; steps run in
+// pairs through it, and an odd last step through the one-step graph.  One graph per device is cached, keyed by every argument but the
 // step count; its split scratch (if any) lives as long as the graph.  When
 // the key changes, the old graph is destroyed (deferred until it finishes)
 // and its scratch freed in stream order behind its last launch.
@@ -366,9 +369,11 @@ struct SimKey {
 struct SimGraph {
     bool valid = false;
     SimKey key = {};
-    cudaGraphExec_t exec = nullptr;
-    void *scratch = nullptr;
-    cudaEvent_t done = nullptr;    // recorded after the latest replay
+    cudaGraphExec_t exec = nullptr;    // one step: forces (+ reduction), then Euler
+    cudaGraphExec_t exec2 = nullptr;   // small N: two steps with Euler fused into the forces
+    void *scratch = nullptr;           // split partials (tiled path)
+    void *pos_b = nullptr;             // second position buffer of the fused steps
+    cudaEvent_t done = nullptr;        // recorded after the latest replay
 };
 
 std::mutex g_sim_mu;
@@ -377,16 +382,38 @@ cudaStream_t g_capture[kMaxDevices] = {};
 
 nbody_status sim_release(SimGraph &g, cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
-    if (g.exec != nullptr) e = cudaGraphExecDestroy(g.exec);
-    if (g.scratch != nullptr) {
-        if (g.done != nullptr) cudaStreamWaitEvent(stream, g.done, 0);
-        const cudaError_t ef = cudaFreeAsync(g.scratch, stream);
-        if (e == cudaSuccess) e = ef;
+    for (cudaGraphExec_t *x : {&g.exec, &g.exec2}) {
+        if (*x != nullptr) {
+            const cudaError_t ex = cudaGraphExecDestroy(*x);
+            if (e == cudaSuccess) e = ex;
+            *x = nullptr;
+        }
     }
-    g.exec = nullptr;
-    g.scratch = nullptr;
+    if ((g.scratch != nullptr || g.pos_b != nullptr) && g.done != nullptr)
+        cudaStreamWaitEvent(stream, g.done, 0);
+    for (void **b : {&g.scratch, &g.pos_b}) {
+        if (*b != nullptr) {
+            const cudaError_t ef = cudaFreeAsync(*b, stream);
+            if (e == cudaSuccess) e = ef;
+            *b = nullptr;
+        }
+    }
     g.valid = false;
     return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
+}
+
+// Capture `body` on the device's capture stream and instantiate it.
+template <typename Body>
+cudaError_t capture_graph(cudaStream_t cap, Body body, cudaGraphExec_t *exec) {
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return e;
+    const cudaError_t el = body(cap);
+    e = cudaStreamEndCapture(cap, &graph);
+    if (el != cudaSuccess) e = el;
+    if (e == cudaSuccess) e = cudaGraphInstantiate(exec, graph, 0);
+    if (graph != nullptr) cudaGraphDestroy(graph);
+    return e;
 }
 
 nbody_status sim_build(int dev_id, DeviceState *dev, const SimKey &k, SimGraph &g,
@@ -409,30 +436,52 @@ nbody_status sim_build(int dev_id, DeviceState *dev, const SimKey &k, SimGraph &
     }
     const cudaStream_t cap = g_capture[dev_id];
     const int ni = static_cast<int>(k.n);
+    float4 *pos = reinterpret_cast<float4 *>(const_cast<float *>(k.pm));
+    float4 *vel = reinterpret_cast<float4 *>(k.vel);
+    float4 *acc = reinterpret_cast<float4 *>(k.acc);
     const nbody::Problem pr = {k.pm, k.pm, ni, ni, k.eps2};
-    cudaGraph_t graph = nullptr;
-    e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
-    if (e == cudaSuccess) {
-        cudaError_t el = launch_planned(plan, pr, reinterpret_cast<float4 *>(k.acc),
-                                        static_cast<float4 *>(scratch), dev->sm_count, cap);
+    cudaGraphExec_t exec = nullptr, exec2 = nullptr;
+    e = capture_graph(cap, [&](cudaStream_t st) {
+        cudaError_t el = launch_planned(plan, pr, acc, static_cast<float4 *>(scratch),
+                                        dev->sm_count, st);
         if (el == cudaSuccess)
-            el = nbody::launch_euler(reinterpret_cast<float4 *>(const_cast<float *>(k.pm)),
-                                     reinterpret_cast<float4 *>(k.vel),
-                                     reinterpret_cast<const float4 *>(k.acc), ni, k.dt,
-                                     dev->sm_count, cap);
-        e = cudaStreamEndCapture(cap, &graph);
-        if (el != cudaSuccess) e = el;
+            el = nbody::launch_euler(pos, vel, acc, ni, k.dt, dev->sm_count, st);
+        return el;
+    }, &exec);
+    // Small N: two steps per replay with the Euler update fused into the
+    // cluster kernel, positions alternating between pos_mass and pos_b.
+    void *pos_b = nullptr;
+    if (e == cudaSuccess && plan.path == NBODY_PATH_CLUSTER) {
+        e = cudaMallocFromPoolAsync(&pos_b, static_cast<size_t>(16 * k.n), dev->pool, stream);
+        if (e == cudaSuccess) {
+            float4 *pb = static_cast<float4 *>(pos_b);
+            const nbody::Problem pr_b = {reinterpret_cast<const float *>(pb),
+                                         reinterpret_cast<const float *>(pb), ni, ni, k.eps2};
+            const int ntiles = static_cast<int>(ceil_div(k.n, plan.tile));
+            const nbody::EulerFuse to_b = {pb, vel, k.dt};
+            const nbody::EulerFuse to_a = {pos, vel, k.dt};
+            e = capture_graph(cap, [&](cudaStream_t st) {
+                cudaError_t el = nbody::launch_cluster(plan.variant, pr, plan.num_iblocks,
+                                                       plan.cluster, plan.tiles_per_split, ntiles,
+                                                       acc, st, &to_b);
+                if (el == cudaSuccess)
+                    el = nbody::launch_cluster(plan.variant, pr_b, plan.num_iblocks, plan.cluster,
+                                               plan.tiles_per_split, ntiles, acc, st, &to_a);
+                return el;
+            }, &exec2);
+        }
     }
-    cudaGraphExec_t exec = nullptr;
-    if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
-    if (graph != nullptr) cudaGraphDestroy(graph);
     if (e != cudaSuccess) {
+        if (exec != nullptr) cudaGraphExecDestroy(exec);
         if (scratch != nullptr) cudaFreeAsync(scratch, stream);
+        if (pos_b != nullptr) cudaFreeAsync(pos_b, stream);
         return cuda_fail(e);
     }
     g.key = k;
     g.exec = exec;
+    g.exec2 = exec2;
     g.scratch = scratch;
+    g.pos_b = pos_b;
     g.valid = true;
     return NBODY_OK;
 }
@@ -530,7 +579,11 @@ nbody_status nbody_simulate(float *pos_mass, float *vel, float *acc_pot, int64_t
         if (g.valid && (st = sim_release(g, stream)) != NBODY_OK) return st;
         if ((st = sim_build(dev_id, dev, key, g, stream)) != NBODY_OK) return st;
     }
-    for (int64_t s = 0; s < steps; ++s)
+    int64_t left = steps;
+    if (g.exec2 != nullptr)
+        for (; left >= 2; left -= 2)
+            if ((e = cudaGraphLaunch(g.exec2, stream)) != cudaSuccess) return cuda_fail(e);
+    for (; left > 0; --left)
         if ((e = cudaGraphLaunch(g.exec, stream)) != cudaSuccess) return cuda_fail(e);
     if ((e = cudaEventRecord(g.done, stream)) != cudaSuccess) return cuda_fail(e);
     return NBODY_OK;

@@ -33,6 +33,16 @@ const TiledVariant &tiled_variant(int v);
 cudaError_t launch_tiled(int variant, const Problem &pr, int num_ib, int splits,
                          int tiles_per_split, int ntiles, float4 *out, cudaStream_t stream);
 
+// Euler update applied by a force kernel as it stores each target's result:
+// pos_out = pos + dt * vel (old vel), then vel += dt * a, every product and
+// sum rounded on its own.  pos_out must not be the targets array (other CTAs
+// are still reading it); the mass is copied.
+struct EulerFuse {
+    float4 *pos_out;
+    float4 *vel;
+    float dt;
+};
+
 // A compiled instantiation of the small-N cluster kernel.
 struct ClusterVariant {
     int i_per_thread;   // K targets per lane (even); the cluster's target block is 32 K
@@ -56,7 +66,8 @@ const ClusterVariant &cluster_variant(int v);
 // cluster b handles targets [b * 32K, (b + 1) * 32K), its CTA of rank c the
 // source tiles [c * tpc, min((c + 1) * tpc, ntiles)).  Writes out[i] directly.
 cudaError_t launch_cluster(int variant, const Problem &pr, int num_ib, int cluster,
-                           int tiles_per_cta, int ntiles, float4 *out, cudaStream_t stream);
+                           int tiles_per_cta, int ntiles, float4 *out, cudaStream_t stream,
+                           const EulerFuse *euler = nullptr);
 
 // out[i] = sum over s of part[s * n + i], in the order s = 0, 1, ..., compensated.
 cudaError_t launch_reduce_splits(const float4 *part, int n, int splits, float4 *out,

@@ -359,7 +359,8 @@ def _separate_steps(w, steps):
     return pm, vel, acc
 
 
-@pytest.mark.parametrize("name,steps", [("smallcube1024", 20), ("plummer65536", 10),
+@pytest.mark.parametrize("name,steps", [("smallcube1024", 20), ("smallcube1024", 7),
+                                        ("smallcube4096", 3), ("plummer65536", 10),
                                         ("clumps200003", 2)])
 def test_simulate_is_the_separate_calls(name, steps):
     w = W.named(name)
