@@ -40,7 +40,7 @@ RECIPE_SM_MAX_MHZ = 2070.0    # fallback if no measured peaks file is present
 KERNEL_SOURCES = ["all_pairs_gravitational_gb300/csrc/forces_tiled.cu",
                   "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"]
 TRAFFIC_BY_SOURCE = {
-    "186a0bef5d143dde": {"bytes": 24.84e6 + 83.25e6,
+    "ed8835a7e0b6f2f8": {"bytes": 25.21e6 + 83.92e6,
                          "profile": "profiles/forces_tiled_plummer1048576_dram.md"},
 }
 
