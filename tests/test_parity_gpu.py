@@ -463,3 +463,32 @@ def test_compensated_precision_parity(name):
     rows = np.arange(w.n) if w.n <= 20000 else sample_rows(w.n, 1500, 4)
     e = assert_parity(got, oracle.forces(w.pos_mass, w.eps2, rows=rows), rows)
     assert e["l2_a"] <= 1e-6 and e["l2_p"] <= 1e-6, e
+
+
+@pytest.mark.slow
+def test_plummer1048576_properties_of_every_output():
+    """All 2^20 outputs of the benchmark workload, through properties that hold
+    at any size: Newton's third law over every body, and the binned radial
+    acceleration and potential of the (r <= 10 truncated) Plummer profile."""
+    w = W.named("plummer1048576")
+    acc = gpu_forces(w.pos_mass, w.eps2).astype(np.float64)
+    assert np.isfinite(acc).all()
+    m = w.pos_mass[:, 3].astype(np.float64)
+    x = w.pos_mass[:, :3].astype(np.float64)
+    total = np.abs((m[:, None] * acc[:, :3]).sum(0)).max()
+    assert total < 1e-6 * (m[:, None] * np.abs(acc[:, :3])).sum()
+    r = np.linalg.norm(x, axis=1)
+    ar = (acc[:, :3] * x).sum(1) / r
+    mass = lambda rr: rr ** 3 / (1.0 + rr * rr) ** 1.5
+    mtrunc = mass(10.0)
+    for lo, hi in [(0.3, 0.6), (0.6, 1.0), (1.0, 2.0), (2.0, 4.0), (4.0, 8.0)]:
+        sel = (r >= lo) & (r < hi)
+        model = -(mass(r[sel]) / mtrunc) / r[sel] ** 2
+        assert abs(ar[sel].mean() / model.mean() - 1.0) < 0.01, (lo, hi)
+    # potential without the self term; the r <= 10 truncated profile has
+    # phi(r) = -[(1 + r^2)^(-1/2) - 101^(-3/2)] / M(10) inside the cut
+    pself = acc[:, 3] + m / np.sqrt(float(w.eps2))
+    for lo, hi in [(0.3, 1.0), (1.0, 3.0), (3.0, 8.0)]:
+        sel = (r >= lo) & (r < hi)
+        model = -(1.0 / np.sqrt(1.0 + r[sel] ** 2) - 101.0 ** -1.5) / mtrunc
+        assert abs(pself[sel].mean() / model.mean() - 1.0) < 0.01, (lo, hi)
