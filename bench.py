@@ -144,23 +144,25 @@ def cpu_model():
     return "unknown"
 
 
-def time_oracle(w, target_seconds, max_rows=None):
+def time_oracle(w, target_seconds, max_rows=None, threads=0):
     """Oracle interactions/s on a sample of target rows x all sources, sized to
-    about target_seconds of work after a short calibration."""
+    about target_seconds of work after a short calibration (threads = 0: all
+    host cores)."""
     import oracle
     n = w.n
-    probe = max(1, min(n, 8 * oracle.max_threads()))
-    oracle.forces(w.pos_mass, w.eps2, rows=range(min(n, oracle.max_threads())))   # wake the threads
+    cores = threads if threads > 0 else oracle.max_threads()
+    probe = max(1, min(n, 8 * cores))
+    oracle.forces(w.pos_mass, w.eps2, rows=range(min(n, cores)), threads=threads)   # wake the threads
     t0 = time.perf_counter()
-    oracle.forces(w.pos_mass, w.eps2, rows=range(probe))
+    oracle.forces(w.pos_mass, w.eps2, rows=range(probe), threads=threads)
     dt = max(time.perf_counter() - t0, 1e-6)
     rows = int(max(probe, min(n, probe * target_seconds / dt)))
     if max_rows:
         rows = min(rows, max_rows)
     t0 = time.perf_counter()
-    oracle.forces(w.pos_mass, w.eps2, rows=range(rows))
+    oracle.forces(w.pos_mass, w.eps2, rows=range(rows), threads=threads)
     el = time.perf_counter() - t0
-    return {"value": rows * n / el, "unit": "interactions/s", "cores": oracle.max_threads(),
+    return {"value": rows * n / el, "unit": "interactions/s", "cores": cores,
             "kind": "oracle", "seconds": el,
             "sample": f"{rows} target rows x all {n} sources of {w.name} (fp64, OpenMP)",
             "cpu_model": cpu_model()}
@@ -538,12 +540,14 @@ def configs_probe(apg, W, device):
         plan = apg.nbody_plan_forces(n, props.multi_processor_count)
         rate = float(n) * n / (ms / 1e3)
         cpu = time_oracle(w, 1.5)
+        cpu1 = time_oracle(w, 0.5, threads=1) if n <= 16384 else None
         out.append({"workload": name, "n": n, "forces_ms": ms, "interactions_per_s": rate,
                     "gflops_20": rate * FLOPS_PER_PAIR / 1e9, "frac_fp32_peak": rate / peak,
                     "simulate_step_ms": step_ms,
                     "path": "cluster" if plan["path"] == 2 else "tiled",
                     "splits": plan["splits"],
-                    "cpu_oracle_interactions_per_s": cpu["value"], "cpu_cores": cpu["cores"]})
+                    "cpu_oracle_interactions_per_s": cpu["value"], "cpu_cores": cpu["cores"],
+                    "cpu_oracle_1thread_interactions_per_s": cpu1["value"] if cpu1 else None})
         del pm, vel, acc
     return out
 
