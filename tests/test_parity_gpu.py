@@ -492,3 +492,73 @@ def test_plummer1048576_properties_of_every_output():
         sel = (r >= lo) & (r < hi)
         model = -(1.0 / np.sqrt(1.0 + r[sel] ** 2) - 101.0 ** -1.5) / mtrunc
         assert abs(pself[sel].mean() / model.mean() - 1.0) < 0.01, (lo, hi)
+
+
+# ------------------------------------------------------------ concurrency
+
+def test_concurrent_host_threads_and_streams():
+    """Four host threads, each with its own stream and problem, call the
+    library at the same time (the C calls run without the GIL): per-device
+    set-up, the split scratch pool and the launches are thread-safe, and
+    each result matches the same call made alone."""
+    import threading
+    sizes = [3001, 20011, 70001, 4096]
+    work = [W.clumps(n, seed=40 + n) for n in sizes]
+    alone = [gpu_forces(w.pos_mass, w.eps2) for w in work]
+    outs = [None] * len(work)
+    errs = []
+
+    def run(k):
+        try:
+            st = torch.cuda.Stream()
+            w = work[k]
+            with torch.cuda.stream(st):
+                pm = torch.from_numpy(w.pos_mass).to(dev(), non_blocking=False)
+                acc = torch.empty_like(pm)
+                for _ in range(3):
+                    apg.nbody_forces(pm, float(w.eps2), acc)
+            st.synchronize()
+            outs[k] = acc.cpu().numpy()
+        except Exception as e:                       # reported below
+            errs.append(e)
+
+    threads = [threading.Thread(target=run, args=(k,)) for k in range(len(work))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errs, errs
+    for k in range(len(work)):
+        assert np.array_equal(outs[k], alone[k]), sizes[k]
+
+
+def test_simulate_from_two_threads_alternately():
+    """nbody_simulate's per-device graph cache under two threads that take
+    turns with different problems: every trajectory equals the separate
+    calls."""
+    import threading
+    wa, wb = W.small_cube(1024), W.plummer(30000, seed=5, eps=0.01)
+    ref = {w.name: _separate_steps(w, 6) for w in (wa, wb)}
+    got = {}
+    lock = threading.Lock()
+
+    def run(w):
+        pm = torch.from_numpy(w.pos_mass).to(dev())
+        vel = torch.from_numpy(w.vel).to(dev())
+        acc = torch.empty_like(pm)
+        st = torch.cuda.Stream()
+        for _ in range(3):
+            with lock:                      # interleave the two problems' calls
+                with torch.cuda.stream(st):
+                    apg.nbody_simulate(pm, vel, acc, float(w.eps2), float(w.dt), 2)
+        st.synchronize()
+        got[w.name] = (pm, vel, acc)
+
+    threads = [threading.Thread(target=run, args=(w,)) for w in (wa, wb)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    for name, (pm, vel, acc) in got.items():
+        assert torch.equal(pm, ref[name][0]) and torch.equal(vel, ref[name][1])
+        assert torch.equal(acc, ref[name][2])
