@@ -6,7 +6,8 @@ The compute path lives in ``libnbody.so`` (hand-written sm_103a CUDA, see
 use.
 """
 from ._binding import (EXPORTS, LIB_PATH, NBODY_NOALLOC_MAX_N, NBODY_PATH_AUTO,
-                       NBODY_PATH_CLUSTER, NBODY_PATH_TILED, NBODY_PRECISION_COMPENSATED,
+                       NBODY_PATH_CLUSTER, NBODY_PATH_SYMMETRIC, NBODY_PATH_TILED,
+                       NBODY_PRECISION_COMPENSATED,
                        NBODY_PRECISION_DEFAULT, NbodyError, load_library,
                        nbody_euler_step, nbody_forces, nbody_forces_ex, nbody_forces_noalloc,
                        nbody_forces_ts,
@@ -14,6 +15,6 @@ from ._binding import (EXPORTS, LIB_PATH, NBODY_NOALLOC_MAX_N, NBODY_PATH_AUTO,
                        nbody_status_string)
 
 __all__ = ["EXPORTS", "LIB_PATH", "NBODY_NOALLOC_MAX_N", "NBODY_PATH_AUTO", "NBODY_PATH_CLUSTER",
-           "NBODY_PATH_TILED", "NBODY_PRECISION_COMPENSATED", "NBODY_PRECISION_DEFAULT", "NbodyError", "load_library", "nbody_euler_step", "nbody_forces",
+           "NBODY_PATH_SYMMETRIC", "NBODY_PATH_TILED", "NBODY_PRECISION_COMPENSATED", "NBODY_PRECISION_DEFAULT", "NbodyError", "load_library", "nbody_euler_step", "nbody_forces",
            "nbody_forces_ex", "nbody_forces_noalloc", "nbody_forces_ts", "nbody_last_cuda_error",
            "nbody_plan_forces", "nbody_simulate", "nbody_status_string"]

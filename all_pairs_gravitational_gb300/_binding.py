@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnbody.so
 NBODY_PATH_AUTO = 0
 NBODY_PATH_TILED = 1
 NBODY_PATH_CLUSTER = 2
+NBODY_PATH_SYMMETRIC = 3
 NBODY_PRECISION_DEFAULT = 0
 NBODY_PRECISION_COMPENSATED = 1
 

@@ -45,47 +45,6 @@ constexpr int kStages = 3;
 // large term exactly enough); it costs 12 fp32 operations per 32 x 13.
 constexpr int kFoldJ = 32;
 
-// Compensated totals of one thread: in registers, or (TSMEM) in shared
-// memory, one column per thread so that a warp's accesses are contiguous.
-// Shared-memory totals free 8 registers per target pair for more
-// instruction-level parallelism at the cost of 4 shared accesses per
-// component per fold.
-template <int KP, int NT, bool TSMEM>
-struct Totals;
-
-template <int KP, int NT>
-struct Totals<KP, NT, false> {
-    f2 h[KP][4], l[KP][4];
-    __device__ __forceinline__ void init() {
-#pragma unroll
-        for (int q = 0; q < KP; ++q)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) h[q][c] = l[q][c] = 0ull;
-    }
-    __device__ __forceinline__ void fold(int q, int c, f2 &part) { f2_kahan_fold(h[q][c], l[q][c], part); }
-    __device__ __forceinline__ f2 value(int q, int c) { return f2_sub(h[q][c], l[q][c]); }
-};
-
-template <int KP, int NT>
-struct Totals<KP, NT, true> {
-    f2 (*s)[NT];     // [KP * 4 * 2][NT]: (hi, lo) of component c of pair q
-    int tid;
-    __device__ __forceinline__ void init() {
-#pragma unroll
-        for (int r = 0; r < KP * 8; ++r) s[r][tid] = 0ull;
-    }
-    __device__ __forceinline__ void fold(int q, int c, f2 &part) {
-        f2 hi = s[(q * 4 + c) * 2][tid];
-        f2 lo = s[(q * 4 + c) * 2 + 1][tid];
-        f2_kahan_fold(hi, lo, part);
-        s[(q * 4 + c) * 2][tid] = hi;
-        s[(q * 4 + c) * 2 + 1][tid] = lo;
-    }
-    __device__ __forceinline__ f2 value(int q, int c) {
-        return f2_sub(s[(q * 4 + c) * 2][tid], s[(q * 4 + c) * 2 + 1][tid]);
-    }
-};
-
 // Loop modes:
 //   0: one source per step of the unrolled loop;
 //   2: two sources per step, their pairs computed side by side (more

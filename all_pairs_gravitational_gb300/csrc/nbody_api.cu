@@ -62,6 +62,7 @@ struct DeviceState {
     int sm_count = 0;
     int tiled_occ[kMaxVariants] = {0};
     int cluster_occ[kMaxVariants] = {0};
+    int sym_occ[kMaxVariants] = {0};
     cudaMemPool_t pool = nullptr;     // stream-ordered scratch for split partials
 };
 
@@ -98,6 +99,15 @@ nbody_status device_state(DeviceState **out) {
             // limited by their shared memory, see plan_cluster_variant)
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.cluster_occ[v], cv.fn_pot,
                                                               cv.warps * 32, 0);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        for (int v = 0; v < nbody::sym_variant_count() && v < kMaxVariants; ++v) {
+            const nbody::SymVariant &sv = nbody::sym_variant(v);
+            if ((e = cudaFuncSetAttribute(sv.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(sv.smem))) != cudaSuccess)
+                return cuda_fail(e);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sym_occ[v], sv.fn, sv.warps * 32,
+                                                              sv.smem);
             if (e != cudaSuccess) return cuda_fail(e);
         }
         cudaMemPoolProps props = {};
@@ -248,29 +258,127 @@ void plan_cluster_variant(int64_t nt, int64_t ns, int sm, int occ, int variant, 
 // tiled one from 8192).
 constexpr int64_t kClusterMaxN = 6144;
 
-nbody_status make_plan(int64_t nt, int64_t ns, int sm, const int *tiled_occ,
-                       const int *cluster_occ, const nbody_forces_opts *opts, nbody_plan *p) {
+// Symmetric path (each unordered pair once).  Smallest n the automatic choice
+// sends to it, its default variant, and the cap on its partials: the j-side
+// partials take (nb - 1) / 2 (+1) records per body, so they grow as n^2 / T.
+constexpr int64_t kSymMinN = 32768;
+constexpr int kDefaultSymVariant = 0;
+constexpr int64_t kMaxSymScratchBytes = int64_t(24) << 30;
+// Relative cost model of the symmetric path: evaluations (two interactions
+// each) per SM-second, the fixed cost of a CTA in evaluations, scratch traffic.
+constexpr double kSymEvalsPerSmSecond = 1.1e10;
+constexpr double kSymItemOverheadEvals = 64.0 * 1024.0;
+
+struct Occupancy {
+    const int *tiled;
+    const int *cluster;
+    const int *sym;
+};
+
+// Block count, j-side slots per body (the largest), and units per row (the
+// largest) of the symmetric decomposition.
+struct SymGeometry {
+    int64_t block, nb, jslots, units;
+};
+
+SymGeometry sym_geometry(const nbody::SymVariant &v, int64_t n) {
+    SymGeometry g;
+    g.block = 32LL * v.warps * v.i_per_thread;
+    g.nb = ceil_div(n, g.block);
+    const int64_t h = (g.nb - 1) / 2;
+    g.jslots = h + (g.nb % 2 == 0 ? 1 : 0);
+    g.units = (1 + g.jslots) * (g.block / v.sub);
+    return g;
+}
+
+bool plan_sym(int64_t n, int sm, int occ, int variant, int splits_req, nbody_plan *p) {
+    const nbody::SymVariant &v = nbody::sym_variant(variant);
+    const SymGeometry g = sym_geometry(v, n);
+    const int64_t jbytes = 16 * g.jslots * n;
+    if (jbytes + 16 * n > kMaxSymScratchBytes) return false;
+    const int64_t slots = static_cast<int64_t>(sm > 0 ? sm : 1) * (occ > 0 ? occ : 1);
+    const double slot_rate = kSymEvalsPerSmSecond / (occ > 0 ? occ : 1);
+    const double unit_evals = static_cast<double>(g.block) * v.sub;
+
+    int64_t s_lo = 1, s_hi = std::min<int64_t>(g.units, kMaxSplits);
+    s_hi = std::max<int64_t>(1, std::min<int64_t>(s_hi, (kMaxSymScratchBytes - jbytes) / (16 * n)));
+    if (splits_req > 0) s_lo = s_hi = std::min<int64_t>(splits_req, g.units);
+
+    double best_t = INFINITY;
+    int64_t best_s = 1, best_upp = g.units, best_waves = 1;
+    for (int64_t s = s_lo; s <= s_hi; ++s) {
+        const int64_t upp = ceil_div(g.units, s);   // units of the largest piece
+        const int64_t waves = ceil_div(g.nb * s, slots);
+        double t = static_cast<double>(waves) * (upp * unit_evals + kSymItemOverheadEvals) /
+                   slot_rate;
+        const bool reduce = s > 1 || g.jslots > 0;
+        if (reduce) t += kLaunchSeconds + 16.0 * (s + g.jslots + 1) * n / kScratchBytesPerSecond;
+        if (t < best_t * (1.0 - 1e-3)) {
+            best_t = t;
+            best_s = s;
+            best_upp = upp;
+            best_waves = waves;
+        }
+    }
+    p->path = NBODY_PATH_SYMMETRIC;
+    p->variant = variant;
+    p->i_per_thread = v.i_per_thread;
+    p->threads = v.warps * 32;
+    p->tile = v.sub;
+    p->num_iblocks = static_cast<int32_t>(g.nb);
+    p->splits = static_cast<int32_t>(best_s);
+    p->tiles_per_split = static_cast<int32_t>(best_upp);
+    p->cluster = 1;
+    p->warps_j = 1;
+    p->grid = g.nb * best_s;
+    p->scratch_bytes = (best_s > 1 || g.jslots > 0) ? 16 * (best_s + g.jslots) * n : 0;
+    p->fill = static_cast<double>(g.nb * best_s) / static_cast<double>(best_waves * slots);
+    return true;
+}
+
+// all_pairs: the targets are the sources (same array, nt == ns), the case the
+// symmetric path needs.
+nbody_status make_plan(int64_t nt, int64_t ns, bool all_pairs, int sm, const Occupancy &occ,
+                       const nbody_forces_opts *opts, nbody_plan *p) {
     if (nt <= 0 || nt > INT32_MAX || ns <= 0 || ns > INT32_MAX || sm <= 0 || p == nullptr)
         return NBODY_ERR_INVALID_ARG;
     nbody_forces_opts o = {NBODY_PATH_AUTO, -1, 0, 0};
     if (opts != nullptr) o = *opts;
-    if (o.path < NBODY_PATH_AUTO || o.path > NBODY_PATH_CLUSTER || o.splits < 0)
+    if (o.path < NBODY_PATH_AUTO || o.path > NBODY_PATH_SYMMETRIC || o.splits < 0)
         return NBODY_ERR_INVALID_ARG;
     if (o.precision < 0 || o.precision > 1) return NBODY_ERR_INVALID_ARG;
     if (o.precision == 1) {   // compensated: the tiled path's compensated kernel
-        if (o.path == NBODY_PATH_CLUSTER || (o.variant >= 0 && o.variant != kCompensatedTiledVariant))
+        if (o.path == NBODY_PATH_CLUSTER || o.path == NBODY_PATH_SYMMETRIC ||
+            (o.variant >= 0 && o.variant != kCompensatedTiledVariant))
             return NBODY_ERR_INVALID_ARG;
         o.path = NBODY_PATH_TILED;
         o.variant = kCompensatedTiledVariant;
     }
+    all_pairs = all_pairs && nt == ns;
+    if (o.path == NBODY_PATH_SYMMETRIC && !all_pairs) return NBODY_ERR_INVALID_ARG;
     int path = o.path;
-    if (path == NBODY_PATH_AUTO)
-        path = (nt <= kClusterMaxN && ns <= kClusterMaxN) ? NBODY_PATH_CLUSTER : NBODY_PATH_TILED;
+    if (path == NBODY_PATH_AUTO) {
+        if (nt <= kClusterMaxN && ns <= kClusterMaxN) {
+            path = NBODY_PATH_CLUSTER;
+        } else if (all_pairs && nt >= kSymMinN &&
+                   plan_sym(nt, sm, occ.sym[kDefaultSymVariant], kDefaultSymVariant, o.splits, p)) {
+            return NBODY_OK;
+        } else {
+            path = NBODY_PATH_TILED;
+        }
+    }
+    if (path == NBODY_PATH_SYMMETRIC) {
+        const int variant = o.variant < 0 ? kDefaultSymVariant : o.variant;
+        if (variant >= nbody::sym_variant_count() || variant >= kMaxVariants)
+            return NBODY_ERR_INVALID_ARG;
+        return plan_sym(nt, sm, occ.sym[variant], variant, o.splits, p) ? NBODY_OK
+                                                                        : NBODY_ERR_INVALID_ARG;
+    }
     if (path == NBODY_PATH_TILED) {
         const int variant = o.variant < 0 ? kDefaultTiledVariant : o.variant;
         if (variant >= nbody::tiled_variant_count() || variant >= kMaxVariants)
             return NBODY_ERR_INVALID_ARG;
-        plan_tiled(nt, ns, sm, tiled_occ[variant], variant, o.splits, p);
+        plan_tiled(nt, ns, sm, occ.tiled[variant], variant, o.splits, p);
         return NBODY_OK;
     }
     if (o.splits != 0) return NBODY_ERR_INVALID_ARG;   // the cluster path plans its own split
@@ -285,7 +393,7 @@ nbody_status make_plan(int64_t nt, int64_t ns, int sm, const int *tiled_occ,
         if (v != only) continue;
         nbody_plan cand;
         double t;
-        plan_cluster_variant(nt, ns, sm, cluster_occ[v], v, &cand, &t);
+        plan_cluster_variant(nt, ns, sm, occ.cluster[v], v, &cand, &t);
         if (t < best * (1.0 - 1e-3)) {
             best = t;
             *p = cand;
@@ -296,9 +404,22 @@ nbody_status make_plan(int64_t nt, int64_t ns, int sm, const int *tiled_occ,
 }
 
 // Launch a planned force evaluation; `scratch` holds plan.scratch_bytes when
-// plan.splits > 1.
+// that is not 0.
 cudaError_t launch_planned(const nbody_plan &plan, const nbody::Problem &pr, float4 *out,
                            float4 *scratch, int sm_count, cudaStream_t stream) {
+    if (plan.path == NBODY_PATH_SYMMETRIC) {
+        const int block = plan.threads * plan.i_per_thread;
+        if (plan.scratch_bytes == 0)   // one block, one piece: no partials
+            return nbody::launch_sym(plan.variant, pr.targets, pr.nt, pr.eps2, plan.num_iblocks, 1,
+                                     out, nullptr, stream);
+        float4 *jpart = scratch + static_cast<int64_t>(plan.splits) * pr.nt;
+        cudaError_t e = nbody::launch_sym(plan.variant, pr.targets, pr.nt, pr.eps2,
+                                          plan.num_iblocks, plan.splits, scratch, jpart, stream);
+        if (e == cudaSuccess)
+            e = nbody::launch_reduce_sym(scratch, plan.splits, jpart, pr.nt, block,
+                                         plan.num_iblocks, out, sm_count, stream);
+        return e;
+    }
     const int ntiles = static_cast<int>(ceil_div(pr.ns, plan.tile));
     if (plan.path == NBODY_PATH_CLUSTER)
         return nbody::launch_cluster(plan.variant, pr, plan.num_iblocks, plan.cluster,
@@ -312,6 +433,10 @@ cudaError_t launch_planned(const nbody_plan &plan, const nbody::Problem &pr, flo
     return e;
 }
 
+Occupancy device_occupancy(const DeviceState *dev) {
+    return {dev->tiled_occ, dev->cluster_occ, dev->sym_occ};
+}
+
 // Launch one planned force evaluation (targets x sources) on `stream`, with
 // its split partials in stream-ordered memory from the device's pool.
 nbody_status run_forces(const nbody::Problem &pr, const nbody_forces_opts *opts, float *result,
@@ -320,13 +445,14 @@ nbody_status run_forces(const nbody::Problem &pr, const nbody_forces_opts *opts,
     nbody_status st = device_state(&dev);
     if (st != NBODY_OK) return st;
     nbody_plan plan;
-    if ((st = make_plan(pr.nt, pr.ns, dev->sm_count, dev->tiled_occ, dev->cluster_occ, opts,
+    const bool all_pairs = pr.targets == pr.sources && pr.nt == pr.ns;
+    if ((st = make_plan(pr.nt, pr.ns, all_pairs, dev->sm_count, device_occupancy(dev), opts,
                         &plan)) != NBODY_OK)
         return st;
     float4 *out = reinterpret_cast<float4 *>(result);
     void *scratch = nullptr;
     cudaError_t e;
-    if (plan.path == NBODY_PATH_TILED && plan.splits > 1) {
+    if (plan.scratch_bytes > 0) {
         e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.scratch_bytes), dev->pool,
                                     stream);
         if (e != cudaSuccess) return cuda_fail(e);
@@ -419,8 +545,8 @@ cudaError_t capture_graph(cudaStream_t cap, Body body, cudaGraphExec_t *exec) {
 nbody_status sim_build(int dev_id, DeviceState *dev, const SimKey &k, SimGraph &g,
                        cudaStream_t stream) {
     nbody_plan plan;
-    nbody_status st = make_plan(k.n, k.n, dev->sm_count, dev->tiled_occ, dev->cluster_occ,
-                                nullptr, &plan);
+    nbody_status st = make_plan(k.n, k.n, true, dev->sm_count, device_occupancy(dev), nullptr,
+                                &plan);
     if (st != NBODY_OK) return st;
     cudaError_t e;
     if (g_capture[dev_id] == nullptr &&
@@ -429,7 +555,7 @@ nbody_status sim_build(int dev_id, DeviceState *dev, const SimKey &k, SimGraph &
     if (g.done == nullptr && (e = cudaEventCreateWithFlags(&g.done, cudaEventDisableTiming)) != cudaSuccess)
         return cuda_fail(e);
     void *scratch = nullptr;
-    if (plan.path == NBODY_PATH_TILED && plan.splits > 1) {
+    if (plan.scratch_bytes > 0) {
         e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.scratch_bytes), dev->pool,
                                     stream);
         if (e != cudaSuccess) return cuda_fail(e);
@@ -519,7 +645,7 @@ int nbody_last_cuda_error(void) { return g_last_cuda_error; }
 
 nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
                                const nbody_forces_opts *opts, nbody_plan *plan) {
-    int occ[kMaxVariants], cocc[kMaxVariants];
+    int occ[kMaxVariants], cocc[kMaxVariants], socc[kMaxVariants];
     for (int v = 0; v < nbody::tiled_variant_count() && v < kMaxVariants; ++v) {
         const nbody::TiledVariant &tv = nbody::tiled_variant(v);
         occ[v] = ctas_per_sm > 0 ? ctas_per_sm : nominal_occ(tv.i_per_thread, tv.threads);
@@ -528,7 +654,14 @@ nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
         const nbody::ClusterVariant &cv = nbody::cluster_variant(v);
         cocc[v] = ctas_per_sm > 0 ? ctas_per_sm : nominal_occ(cv.i_per_thread, cv.warps * 32);
     }
-    return make_plan(n, n, sm_count, occ, cocc, opts, plan);
+    for (int v = 0; v < nbody::sym_variant_count() && v < kMaxVariants; ++v) {
+        const nbody::SymVariant &sv = nbody::sym_variant(v);
+        const int by_smem = static_cast<int>(kSmemPerSm / static_cast<int64_t>(sv.smem + 1024));
+        socc[v] = ctas_per_sm > 0 ? ctas_per_sm
+                                  : std::max(1, std::min(nominal_occ(sv.i_per_thread, sv.warps * 32),
+                                                         by_smem));
+    }
+    return make_plan(n, n, true, sm_count, Occupancy{occ, cocc, socc}, opts, plan);
 }
 
 nbody_status nbody_forces_ex(const float *pos_mass, int64_t n, float eps2, float *acc_pot,

@@ -69,6 +69,29 @@ cudaError_t launch_cluster(int variant, const Problem &pr, int num_ib, int clust
                            int tiles_per_cta, int ntiles, float4 *out, cudaStream_t stream,
                            const EulerFuse *euler = nullptr);
 
+// A compiled instantiation of the symmetric (each unordered pair once) kernel.
+struct SymVariant {
+    int i_per_thread;   // K targets per lane (even)
+    int warps;          // W warps per CTA; a block is T = 32 W K bodies
+    int sub;            // sources per unit (a barrier and a j-side write-back per unit)
+    size_t smem;        // dynamic shared memory per CTA
+    const void *fn;
+};
+
+int sym_variant_count();
+const SymVariant &sym_variant(int v);
+
+// Symmetric kernel over grid = nb * splits CTAs, nb = ceil(n / T): CTA b
+// takes row b % nb, piece b / nb of that row's units.  Writes the i-side
+// partials ipart[piece * n + i] and the j-side partials jpart[(d - 1) * n + j].
+cudaError_t launch_sym(int variant, const float *bodies, int n, float eps2, int nb, int splits,
+                       float4 *ipart, float4 *jpart, cudaStream_t stream);
+
+// out[i] = the splits i-side slots of body i, then its j-side slots, in a
+// fixed order, compensated (block = T bodies).
+cudaError_t launch_reduce_sym(const float4 *ipart, int splits, const float4 *jpart, int n,
+                              int block, int nb, float4 *out, int sm_count, cudaStream_t stream);
+
 // out[i] = sum over s of part[s * n + i], in the order s = 0, 1, ..., compensated.
 cudaError_t launch_reduce_splits(const float4 *part, int n, int splits, float4 *out,
                                  int sm_count, cudaStream_t stream);

@@ -65,7 +65,9 @@ typedef enum nbody_status {
  * folded into compensated (Kahan) totals; a run is bit-reproducible for the
  * same n, inputs and GPU model.  Large n may split the source range over
  * CTAs and add the fp32 partials in a fixed order in a second kernel; the
- * partials live in stream-ordered memory from a library-owned pool.
+ * partials live in stream-ordered memory from a library-owned pool.  From
+ * n = 32768 each unordered pair is evaluated once for both bodies (the
+ * symmetric path below).
  *
  * Errors: NBODY_ERR_INVALID_ARG, _MISALIGNED, _ALIAS (host checks, nothing
  * launched); NBODY_ERR_DEVICE; NBODY_ERR_CUDA.
@@ -145,13 +147,33 @@ int nbody_last_cuda_error(void);
 enum {
     NBODY_PATH_AUTO = 0,     /* the library's choice from n and the SM count */
     NBODY_PATH_TILED = 1,    /* i-blocks x j-splits over the whole grid (any n) */
-    NBODY_PATH_CLUSTER = 2   /* small n: warps and a CTA cluster split j, DSMEM reduction */
+    NBODY_PATH_CLUSTER = 2,  /* small n: warps and a CTA cluster split j, DSMEM reduction */
+    NBODY_PATH_SYMMETRIC = 3 /* all-pairs only: each unordered pair evaluated once and
+                                applied to both bodies (see below) */
 };
+
+/*
+ * The symmetric path.  The pull of j on i and of i on j share r, |r|^2 + eps^2
+ * and its rsqrt (Newton's third law), so one evaluation of the pair law
+ * serves both bodies: 18 fp32 operations per unordered pair instead of 2 x 13.
+ * The pages' kernels evaluate every ordered pair; the sums are the same up to
+ * rounding order, and parity with them is held to the same bounds.  Bodies
+ * are cut into nb blocks of T = 32 * warps * i_per_thread; block pairs at
+ * circular distance 1..(nb-1)/2 (and nb/2 once, for even nb) are evaluated
+ * both ways, each block against itself one way.  The partials (S per body
+ * for the i-side, about nb/2 per body for the j-side, n * 16 bytes each) come
+ * from the library's pool and are added in a fixed order: results are
+ * bit-reproducible.  It needs targets == sources (nbody_forces, or
+ * nbody_forces_ts with the same array and nt == ns), default precision, and
+ * partials within 24 GiB (n up to about 2.5 million); automatic planning uses
+ * it for n >= 32768 when those hold.
+ */
 
 typedef struct nbody_forces_opts {
     int32_t path;       /* NBODY_PATH_* */
     int32_t variant;    /* kernel variant of the path; -1 = library default */
-    int32_t splits;     /* tiled path: j-splits S (0 = planner's choice, 1 = none) */
+    int32_t splits;     /* tiled and symmetric paths: pieces S of the source range
+                           (0 = planner's choice, 1 = none) */
     int32_t precision;  /* NBODY_PRECISION_* */
 } nbody_forces_opts;
 
@@ -169,18 +191,19 @@ enum {
 
 /* The decomposition nbody_forces would launch; host-only, needs no GPU. */
 typedef struct nbody_plan {
-    int32_t path;            /* NBODY_PATH_TILED or NBODY_PATH_CLUSTER */
+    int32_t path;            /* NBODY_PATH_TILED, _CLUSTER or _SYMMETRIC */
     int32_t variant;         /* kernel variant index of that path */
     int32_t i_per_thread;    /* target bodies held in registers by each thread */
     int32_t threads;         /* threads per CTA computing pairs */
-    int32_t tile;            /* source bodies per shared-memory tile */
-    int32_t num_iblocks;     /* CTAs along the targets */
+    int32_t tile;            /* source bodies per shared-memory tile (symmetric: per unit) */
+    int32_t num_iblocks;     /* CTAs along the targets (symmetric: the nb blocks) */
     int32_t splits;          /* pieces of the source range (S) */
-    int32_t tiles_per_split; /* tiled path: source tiles per piece */
+    int32_t tiles_per_split; /* tiled path: source tiles per piece; symmetric: units of
+                                the largest piece */
     int32_t cluster;         /* cluster path: CTAs per cluster */
     int32_t warps_j;         /* cluster path: warps splitting j inside a CTA */
     int64_t grid;            /* CTAs launched by the force kernel */
-    int64_t scratch_bytes;   /* stream-ordered scratch for the partials (0 if S == 1) */
+    int64_t scratch_bytes;   /* stream-ordered scratch for the partials (0 if none) */
     double fill;             /* predicted fraction of CTA slots doing useful work */
 } nbody_plan;
 

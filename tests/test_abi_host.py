@@ -132,6 +132,9 @@ def _covers(plan, n):
     """Every target in exactly one target block, every source tile in exactly
     one piece of the source range."""
     ntiles = -(-n // plan["tile"])
+    if plan["path"] == apg.NBODY_PATH_SYMMETRIC:
+        _sym_covers(plan, n)
+        return
     if plan["path"] == apg.NBODY_PATH_TILED:
         bi = plan["threads"] * plan["i_per_thread"]
         tps, s = plan["tiles_per_split"], plan["splits"]
@@ -153,6 +156,80 @@ def _covers(plan, n):
     assert 0 < plan["fill"] <= 1.0
 
 
+def _sym_units(nb):
+    """Block pairs of the symmetric decomposition, as the header states it:
+    row I takes its own block one way (d = 0) and blocks I + d (mod nb) both
+    ways for 1 <= d <= (nb - 1) / 2, plus d = nb / 2 for I < nb / 2 when nb
+    is even."""
+    h = (nb - 1) // 2
+    rows = []
+    for i in range(nb):
+        ds = list(range(0, h + 1)) + ([nb // 2] if nb % 2 == 0 and i < nb // 2 else [])
+        rows.append([(i, (i + d) % nb, d) for d in ds])
+    return rows
+
+
+@pytest.mark.parametrize("nb", list(range(1, 40)) + [64, 127, 128, 512, 513])
+def test_symmetric_decomposition_meets_every_pair_once(nb):
+    seen = {}
+    for row in _sym_units(nb):
+        for i, j, d in row:
+            if d == 0:
+                assert i == j
+                seen[(i, i)] = seen.get((i, i), 0) + 1
+            else:
+                for key in ((i, j), (j, i)):           # one evaluation, both ways
+                    seen[key] = seen.get(key, 0) + 1
+    assert len(seen) == nb * nb and set(seen.values()) == {1}
+    # j-side slot d - 1 of every body is written by exactly one row
+    slots = {}
+    for row in _sym_units(nb):
+        for i, j, d in row:
+            if d:
+                slots[(j, d - 1)] = slots.get((j, d - 1), 0) + 1
+    assert set(slots.values()) <= {1}
+    h = (nb - 1) // 2
+    for j in range(nb):
+        want = h + (1 if nb % 2 == 0 and j >= nb // 2 else 0)
+        assert sorted(s for (b, s) in slots if b == j) == list(range(want))
+
+
+def _sym_covers(plan, n):
+    t = plan["threads"] * plan["i_per_thread"]
+    nb = plan["num_iblocks"]
+    assert nb == -(-n // t) and t % plan["tile"] == 0 and plan["tile"] % 32 == 0
+    jslots = (nb - 1) // 2 + (1 if nb % 2 == 0 else 0)
+    units = (1 + jslots) * (t // plan["tile"])
+    s, upp = plan["splits"], plan["tiles_per_split"]
+    assert 1 <= s <= units and upp == -(-units // s)
+    assert plan["grid"] == nb * s < 2 ** 31
+    want = 16 * (s + jslots) * n if (s > 1 or jslots > 0) else 0
+    assert plan["scratch_bytes"] == want <= 24 << 30
+    assert 0 < plan["fill"] <= 1.0
+
+
+@pytest.mark.parametrize("n", [1, 2, 33, 2048, 2049, 4096, 4097, 20011, 32768, 65537, 200003,
+                               1048576, 2 ** 21])
+@pytest.mark.parametrize("splits", [0, 1, 3, 64])
+def test_symmetric_plan(lib, n, splits):
+    plan = apg.nbody_plan_forces(n, 152, path=apg.NBODY_PATH_SYMMETRIC, splits=splits)
+    assert plan["path"] == apg.NBODY_PATH_SYMMETRIC
+    _sym_covers(plan, n)
+    if splits:
+        units = plan["tiles_per_split"] * plan["splits"]
+        assert plan["splits"] == min(splits, units) or plan["splits"] == splits
+
+
+def test_symmetric_plan_limits():
+    with pytest.raises(apg.NbodyError):      # j-side partials beyond 24 GiB
+        apg.nbody_plan_forces(2 ** 23, 152, path=apg.NBODY_PATH_SYMMETRIC)
+    with pytest.raises(apg.NbodyError):      # the compensated kernel is tiled only
+        apg.nbody_plan_forces(65536, 152, path=apg.NBODY_PATH_SYMMETRIC,
+                              precision=apg.NBODY_PRECISION_COMPENSATED)
+    # automatic planning falls back to the tiled path where the partials do not fit
+    assert apg.nbody_plan_forces(2 ** 23, 152)["path"] == apg.NBODY_PATH_TILED
+
+
 @pytest.mark.parametrize("n", [1, 2, 3, 31, 33, 127, 128, 129, 255, 257, 1000, 1024, 4096,
                                16384, 65536, 200003, 1048576, 2 ** 24 + 3, 2 ** 31 - 1])
 @pytest.mark.parametrize("sm", [1, 148, 152, 160])
@@ -162,11 +239,14 @@ def test_plan_covers_all_pairs(lib, n, sm):
 
 
 def test_plan_fills_the_gpu_at_one_million():
-    plan = apg.nbody_plan_forces(1048576, 152)
-    assert plan["fill"] > 0.97
-    one = apg.nbody_plan_forces(1048576, 152, splits=1)
-    assert one["splits"] == 1 and one["scratch_bytes"] == 0
-    assert plan["fill"] > one["fill"]
+    for path in (apg.NBODY_PATH_TILED, apg.NBODY_PATH_SYMMETRIC):
+        plan = apg.nbody_plan_forces(1048576, 152, path=path)
+        assert plan["fill"] > 0.97
+        one = apg.nbody_plan_forces(1048576, 152, path=path, splits=1)
+        assert one["splits"] == 1
+        assert plan["fill"] > one["fill"]
+    one = apg.nbody_plan_forces(1048576, 152, path=apg.NBODY_PATH_TILED, splits=1)
+    assert one["scratch_bytes"] == 0
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 33, 127, 129, 1000, 1024, 2048, 4096, 8192, 12288, 16384])
@@ -182,7 +262,9 @@ def test_auto_path_choice():
     assert apg.nbody_plan_forces(1024, 152)["path"] == apg.NBODY_PATH_CLUSTER
     assert apg.nbody_plan_forces(4096, 152)["path"] == apg.NBODY_PATH_CLUSTER
     assert apg.nbody_plan_forces(8192, 152)["path"] == apg.NBODY_PATH_TILED
-    assert apg.nbody_plan_forces(1048576, 152)["path"] == apg.NBODY_PATH_TILED
+    assert apg.nbody_plan_forces(32767, 152)["path"] == apg.NBODY_PATH_TILED
+    assert apg.nbody_plan_forces(32768, 152)["path"] == apg.NBODY_PATH_SYMMETRIC
+    assert apg.nbody_plan_forces(1048576, 152)["path"] == apg.NBODY_PATH_SYMMETRIC
     with pytest.raises(apg.NbodyError):
         apg.nbody_plan_forces(1000, 152, path=apg.NBODY_PATH_CLUSTER, splits=3)
     with pytest.raises(apg.NbodyError):

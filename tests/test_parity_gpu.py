@@ -186,8 +186,8 @@ def test_forced_plans(variant, splits):
     assert_parity(got, ref)
 
 
-@pytest.mark.parametrize("path", [1, 2])
-def test_disk_near_neighbours_both_paths(path):
+@pytest.mark.parametrize("path", [1, 2, 3])
+def test_disk_near_neighbours_all_paths(path):
     """The disk workload has bodies whose nearest neighbours contribute terms
     hundreds of times |a_i| (condition number ~1e3): the per-body bound holds."""
     w = W.named("disk4096")
@@ -292,6 +292,81 @@ def test_euler_large_bit_exact():
     pm_ref, v_ref = oracle.euler(w.pos_mass, w.vel, acc, w.dt)
     assert np.array_equal(pm.cpu().numpy(), pm_ref)
     assert np.array_equal(vel.cpu().numpy(), v_ref)
+
+
+# ------------------------------------------------------------ symmetric path
+
+SYM = 3   # NBODY_PATH_SYMMETRIC
+
+
+def _sym_block(variant=0):
+    plan = apg.nbody_plan_forces(4096, 152, path=SYM, variant=variant)
+    return plan["threads"] * plan["i_per_thread"]
+
+
+# T = 2048 for the default variant: one block, two (the even extra distance),
+# three, five and eight blocks, each with a ragged last block.
+@pytest.mark.parametrize("n", [1, 2, 33, 1000, 2048, 2049, 4095, 4096, 4097, 6144, 9000, 10240,
+                               16383, 20011])
+def test_symmetric_path_parity(n):
+    w = W.clumps(n, seed=n + 101)
+    got = gpu_forces(w.pos_mass, w.eps2, path=SYM)
+    assert_parity(got, oracle.forces(w.pos_mass, w.eps2))
+
+
+@pytest.mark.parametrize("variant", range(_variant_count(SYM)))
+@pytest.mark.parametrize("splits", [0, 1, 2, 5, 17, 1000])
+def test_symmetric_variants_and_splits(variant, splits):
+    n = 3 * _sym_block(variant) + 77                      # four blocks (even), ragged
+    w = W.cube(n, seed=variant * 100 + splits)
+    got = gpu_forces(w.pos_mass, w.eps2, path=SYM, variant=variant, splits=splits)
+    assert_parity(got, oracle.forces(w.pos_mass, w.eps2))
+
+
+@pytest.mark.parametrize("n,splits", [(32768, 0), (65537, 0), (65537, 1), (131072, 0),
+                                      (262147, 0), (1048576, 0)])
+def test_symmetric_path_counts_every_pair_once(n, splits):
+    """Unit masses and eps^2 = 2^40: |r|^2 < 12 vanishes against 2^40 in fp32,
+    so every potential term is the same value t, the kernel's rsqrt(2^40)
+    (2^-20 up to the hardware rsqrt's error).  Then -p_i / t counts the
+    bodies that body i met, and a block pair skipped or evaluated twice moves
+    that count by at least one for every body involved.  When t is exactly
+    2^-20 every partial sum is exact and the count must be n exactly."""
+    one = gpu_forces(np.array([[0.5, 0.5, 0.5, 1.0]], np.float32), 2.0 ** 40, path=SYM)
+    t = -float(one[0, 3])
+    assert abs(t * 2.0 ** 20 - 1.0) < 2.0 ** -21
+    pm = np.zeros((n, 4), np.float32)
+    pm[:, :3] = W.Stream(n).uniform(3 * n, -1.0, 1.0).reshape(n, 3)
+    pm[:, 3] = 1.0
+    got = gpu_forces(pm, 2.0 ** 40, path=SYM, splits=splits).astype(np.float64)
+    assert np.isfinite(got).all()
+    count = -got[:, 3] / t
+    if t == 2.0 ** -20:
+        assert np.array_equal(count, np.full(n, float(n))), (count.min(), count.max())
+    else:   # fp32 sums of an inexact t: rounding well below one count
+        assert np.abs(count - n).max() < 0.25, (count.min(), count.max())
+
+
+def test_symmetric_path_deterministic_and_ts_identical():
+    w = W.clumps(70001, seed=9)
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    a = apg.nbody_forces_ex(pm, float(w.eps2), path=SYM)
+    for _ in range(2):
+        assert torch.equal(apg.nbody_forces_ex(pm, float(w.eps2), path=SYM), a)
+    assert torch.equal(apg.nbody_forces(pm, float(w.eps2)), a)        # automatic choice
+    assert torch.equal(apg.nbody_forces_ts(pm, pm, float(w.eps2)), a)  # same array
+    torch.cuda.synchronize()
+
+
+def test_symmetric_path_needs_one_array():
+    """The target/source form with distinct arrays never takes the symmetric
+    path: with a copy of the bodies as sources it matches the oracle too."""
+    w = W.clumps(40000, seed=12)
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    out = apg.nbody_forces_ts(pm, pm.clone(), float(w.eps2))
+    torch.cuda.synchronize()
+    rows = sample_rows(w.n, 1500, 3)
+    assert_parity(out.cpu().numpy()[rows], oracle.forces(w.pos_mass, w.eps2, rows=rows))
 
 
 # ------------------------------------------------------------ target/source form
