@@ -294,15 +294,22 @@ __global__ void reduce_sym_kernel(const float4 *__restrict__ ipart, int splits,
 
 // Instantiated shapes: K targets per lane, W warps per CTA, SUB sources per
 // unit, the minimum resident CTAs per SM asked of the register allocator, and
-// the unroll factor of the 32-step chunk loop.
+// the unroll factor of the 32-step chunk loop.  Variant 0 is the default, the
+// fastest measured on GB300 from N = 65536 to 2^20 (3.23e12 interactions/s at
+// 2^20; FMA pipe about 75 % busy, 125 registers, 2 CTAs per SM).  Measured
+// and dropped: two partners per step side by side (K = 4, 6, 8: 1-9 %
+// slower), 1/d^2 from a MUFU reciprocal instead of a packed multiply (one
+// FMA-pipe operation fewer per pair, 2.5 % slower), 3 CTAs per SM at K = 4
+// (12 % slower), 32-body units (1-3 % slower).
 #define NBODY_SYM_LIST(X)                 \
-    X(8, 8, 128, 2, 2)   /* 0: default */ \
-    X(4, 8, 128, 2, 4)   /* 1 */          \
+    X(8, 8, 64, 2, 2)    /* 0: default */ \
+    X(8, 8, 128, 2, 2)   /* 1 */          \
     X(8, 4, 128, 4, 2)   /* 2 */          \
-    X(6, 8, 128, 2, 2)   /* 3 */
+    X(6, 8, 64, 2, 2)    /* 3 */          \
+    X(4, 8, 64, 2, 2)    /* 4 */
 
-#define NBODY_SYM_ENTRY(K, W, SUB, MINB, U)                                        \
-    {K, W, SUB, SymShape<K, W, SUB>::smem_bytes,                                   \
+#define NBODY_SYM_ENTRY(K, W, SUB, MINB, U)                                  \
+    {K, W, SUB, MINB, SymShape<K, W, SUB>::smem_bytes,                             \
      reinterpret_cast<const void *>(&forces_sym_kernel<K, W, SUB, MINB, U>)},
 
 const SymVariant kSymVariants[] = {NBODY_SYM_LIST(NBODY_SYM_ENTRY)};

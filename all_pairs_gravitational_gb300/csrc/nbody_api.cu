@@ -259,9 +259,11 @@ void plan_cluster_variant(int64_t nt, int64_t ns, int sm, int occ, int variant, 
 constexpr int64_t kClusterMaxN = 6144;
 
 // Symmetric path (each unordered pair once).  Smallest n the automatic choice
-// sends to it, its default variant, and the cap on its partials: the j-side
-// partials take (nb - 1) / 2 (+1) records per body, so they grow as n^2 / T.
-constexpr int64_t kSymMinN = 32768;
+// sends to it (measured on GB300: 2.48e12 against the tiled path's 2.25e12
+// interactions/s at 24576 bodies, 1.90e12 against 2.15e12 at 16384), its
+// default variant, and the cap on its partials: the j-side partials take
+// (nb - 1) / 2 (+1) records per body, so they grow as n^2 / T.
+constexpr int64_t kSymMinN = 24576;
 constexpr int kDefaultSymVariant = 0;
 constexpr int64_t kMaxSymScratchBytes = int64_t(24) << 30;
 // Relative cost model of the symmetric path: evaluations (two interactions
@@ -657,9 +659,7 @@ nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
     for (int v = 0; v < nbody::sym_variant_count() && v < kMaxVariants; ++v) {
         const nbody::SymVariant &sv = nbody::sym_variant(v);
         const int by_smem = static_cast<int>(kSmemPerSm / static_cast<int64_t>(sv.smem + 1024));
-        socc[v] = ctas_per_sm > 0 ? ctas_per_sm
-                                  : std::max(1, std::min(nominal_occ(sv.i_per_thread, sv.warps * 32),
-                                                         by_smem));
+        socc[v] = ctas_per_sm > 0 ? ctas_per_sm : std::max(1, std::min(sv.min_ctas, by_smem));
     }
     return make_plan(n, n, true, sm_count, Occupancy{occ, cocc, socc}, opts, plan);
 }

@@ -74,6 +74,7 @@ struct SymVariant {
     int i_per_thread;   // K targets per lane (even)
     int warps;          // W warps per CTA; a block is T = 32 W K bodies
     int sub;            // sources per unit (a barrier and a j-side write-back per unit)
+    int min_ctas;       // resident CTAs per SM the register allocation was bounded for
     size_t smem;        // dynamic shared memory per CTA
     const void *fn;
 };

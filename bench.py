@@ -30,18 +30,25 @@ sys.path.insert(0, ROOT)
 
 METRIC = "interactions/s & GFLOP/s (20 flop/pair) at N=1M fp32, % of FP32/MUFU roofline"
 FLOPS_PER_PAIR = 20           # the pages' pair count (bodyBodyInteraction annotation)
-FP32_OPS_PER_PAIR = 13        # fp32 lane operations the pair law executes (a + p)
+FP32_OPS_PER_PAIR = 13        # fp32 lane operations of the pair law for one ordered pair (a + p)
+SYM_OPS_PER_PAIR = 18         # fp32 lane operations for one unordered pair, both bodies' a + p
 FP32_LANES_PER_SM_CLK = 128
 RECIPE_SM_MAX_MHZ = 2070.0    # fallback if no measured peaks file is present
+PATH_SYMMETRIC = 3
+PATH_NAMES = {1: "tiled", 2: "cluster", 3: "symmetric"}
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the force kernel at N = 2^20, from one ncu capture, keyed by a hash of the
 # kernel's source files: a changed kernel reports null until it is re-measured.
-KERNEL_SOURCES = ["all_pairs_gravitational_gb300/csrc/forces_tiled.cu",
-                  "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"]
+KERNEL_SOURCES = {
+    "tiled": ["all_pairs_gravitational_gb300/csrc/forces_tiled.cu",
+              "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"],
+    "symmetric": ["all_pairs_gravitational_gb300/csrc/forces_sym.cu",
+                  "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"],
+}
 TRAFFIC_BY_SOURCE = {
-    "ed8835a7e0b6f2f8": {"bytes": 25.21e6 + 83.92e6,
-                         "profile": "profiles/forces_tiled_plummer1048576_dram.md"},
+    "b76a733875a3fee3": {"bytes": 419.60e6 + 4.56e9,
+                         "profile": "profiles/forces_sym_plummer1048576_dram.md"},
 }
 
 
@@ -63,10 +70,10 @@ def parse():
     return ap.parse_args()
 
 
-def kernel_source_hash():
+def kernel_source_hash(kind):
     import hashlib
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -96,7 +103,7 @@ def small_n_sweep(apg, W, device, sizes=(1024, 2048, 4096, 8192), reps=20):
         out.append({"n": n, "forces_us": round(best * 1e3, 2),
                     "interactions_per_s": float(n) * n / (best / 1e3),
                     "simulate_us_per_step": round(a.elapsed_time(b) * 1e3 / steps, 2),
-                    "path": "cluster" if plan["path"] == 2 else "tiled",
+                    "path": PATH_NAMES[plan["path"]],
                     "cluster": plan["cluster"], "splits": plan["splits"]})
     return out
 
@@ -123,6 +130,31 @@ def euler_hbm_probe(apg, device, n=1 << 26, reps=5):
     del pm, vel, acc, flush
     torch.cuda.empty_cache()
     return {"n": n, "ms": ms, "bytes": 80 * n, "gbs": 80 * n / (ms / 1e3) / 1e9}
+
+
+def force_roofline(plan, n, sm, sm_max_mhz):
+    """Arithmetic bound of the planned force kernel, in interactions/s.
+
+    Ordered-pair kernels (tiled, cluster) execute 13 fp32 lane operations per
+    interaction.  The symmetric kernel executes 18 per unordered pair, which
+    serves two interactions, except on the nb diagonal blocks, which it
+    evaluates one way (13 per ordered pair).  The bound is the FMA pipe's
+    lane rate over the launch's lane operations, times its N^2 interactions."""
+    lanes_per_s = sm * sm_max_mhz * 1e6 * FP32_LANES_PER_SM_CLK
+    pairs = float(n) * float(n)
+    if plan["path"] == PATH_SYMMETRIC:
+        t = plan["threads"] * plan["i_per_thread"]
+        nb = plan["num_iblocks"]
+        last = n - (nb - 1) * t
+        diag = float((nb - 1) * t * t + last * last)
+        ops = SYM_OPS_PER_PAIR / 2.0 * (pairs - diag) + FP32_OPS_PER_PAIR * diag
+        kind, kernel = "symmetric", "forces_sym_kernel (+ reduce_sym_kernel)"
+    else:
+        ops = FP32_OPS_PER_PAIR * pairs
+        kind, kernel = "tiled", "forces_tiled_kernel (+ split reduction)"
+    return {"peak": lanes_per_s * pairs / ops, "ops_per_interaction": ops / pairs,
+            "kind": kind, "kernel": kernel,
+            "ordered_pair_peak": lanes_per_s / FP32_OPS_PER_PAIR}
 
 
 def measured_peaks():
@@ -324,7 +356,7 @@ def run_ours(args):
     n = w.n
     pairs = float(n) * float(n)
     plan = apg.nbody_plan_forces(n, props.multi_processor_count)
-    launches_per_step = (2 if plan["splits"] > 1 else 1) + 1
+    launches_per_step = (2 if plan["scratch_bytes"] > 0 else 1) + 1
 
     pm0 = torch.from_numpy(w.pos_mass).to(device)
     vel0 = torch.from_numpy(w.vel).to(device)
@@ -368,7 +400,8 @@ def run_ours(args):
 
     peaks, peaks_src = measured_peaks()
     sm_max = float(peaks.get("sm_max_mhz", RECIPE_SM_MAX_MHZ))
-    peak_pairs = props.multi_processor_count * sm_max * 1e6 * FP32_LANES_PER_SM_CLK / FP32_OPS_PER_PAIR
+    roof = force_roofline(plan, n, props.multi_processor_count, sm_max)
+    peak_pairs = roof["peak"]
     forces_s = statistics.mean(forces_ms) / 1e3
     achieved = pairs / forces_s
     euler_s = statistics.mean(euler_ms) / 1e3
@@ -386,7 +419,7 @@ def run_ours(args):
 
     sweep = None if args.no_small_n else small_n_sweep(apg, W, device)
     euler_hbm = None if args.no_small_n else euler_hbm_probe(apg, device)
-    src_hash = kernel_source_hash()
+    src_hash = kernel_source_hash(roof["kind"])
     traffic = TRAFFIC_BY_SOURCE.get(src_hash) if w.name == "plummer1048576" else None
 
     sm_at_clock = clocks.get("sm_mhz")
@@ -408,8 +441,9 @@ def run_ours(args):
                    "step": "nbody_forces (a + p) then nbody_euler_step",
                    "l2": "flushed (256 MiB write) before each timed step, outside its events",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "plan": {k: plan[k] for k in ("variant", "i_per_thread", "threads", "tile",
-                                                 "num_iblocks", "splits", "grid", "fill")}},
+                   "plan": {k: plan[k] for k in ("path", "variant", "i_per_thread", "threads",
+                                                 "tile", "num_iblocks", "splits", "grid",
+                                                 "scratch_bytes", "fill")}},
         "roofline": {
             "bound": "alu",
             "achieved": achieved,
@@ -419,9 +453,14 @@ def run_ours(args):
             "traffic": traffic["bytes"] if traffic else None,
             "traffic_source": (traffic["profile"] if traffic else
                                f"not measured for kernel source {src_hash}"),
-            "kernel": "forces_tiled_kernel (+ split reduction)",
+            "kernel": roof["kernel"],
             "peak_basis": (f"{props.multi_processor_count} SMs x {sm_max:.0f} MHz ({peaks_src}) x "
-                           f"{FP32_LANES_PER_SM_CLK} fp32 lanes / {FP32_OPS_PER_PAIR} fp32 ops per pair"),
+                           f"{FP32_LANES_PER_SM_CLK} fp32 lanes / "
+                           f"{roof['ops_per_interaction']:.4f} fp32 ops per interaction"
+                           + (f" ({SYM_OPS_PER_PAIR} per unordered pair for both bodies, "
+                              f"{FP32_OPS_PER_PAIR} per ordered pair on the diagonal blocks)"
+                              if roof["kind"] == "symmetric" else "")),
+            "frac_of_ordered_pair_bound": achieved / roof["ordered_pair_peak"],
             "frac_at_sampled_clock": (achieved / (peak_pairs * sm_at_clock / sm_max)
                                       if sm_at_clock else None),
             "forces_ms": statistics.mean(forces_ms),
@@ -516,8 +555,7 @@ def configs_probe(apg, W, device):
     import torch
     props = torch.cuda.get_device_properties(device)
     peaks, _ = measured_peaks()
-    peak = props.multi_processor_count * float(peaks.get("sm_max_mhz", RECIPE_SM_MAX_MHZ)) * 1e6 * \
-        FP32_LANES_PER_SM_CLK / FP32_OPS_PER_PAIR
+    sm_max = float(peaks.get("sm_max_mhz", RECIPE_SM_MAX_MHZ))
     out = []
     for name in W.CONFIG_NAMES + [f"smallcube{n}" for n in W.SMALL_SWEEP]:
         w = W.named(name)
@@ -538,13 +576,15 @@ def configs_probe(apg, W, device):
         b.synchronize()
         step_ms = a.elapsed_time(b) / steps
         plan = apg.nbody_plan_forces(n, props.multi_processor_count)
+        roof = force_roofline(plan, n, props.multi_processor_count, sm_max)
         rate = float(n) * n / (ms / 1e3)
         cpu = time_oracle(w, 1.5)
         cpu1 = time_oracle(w, 0.5, threads=1) if n <= 16384 else None
         out.append({"workload": name, "n": n, "forces_ms": ms, "interactions_per_s": rate,
-                    "gflops_20": rate * FLOPS_PER_PAIR / 1e9, "frac_fp32_peak": rate / peak,
+                    "gflops_20": rate * FLOPS_PER_PAIR / 1e9, "frac_fp32_peak": rate / roof["peak"],
+                    "frac_of_ordered_pair_bound": rate / roof["ordered_pair_peak"],
                     "simulate_step_ms": step_ms,
-                    "path": "cluster" if plan["path"] == 2 else "tiled",
+                    "path": PATH_NAMES[plan["path"]],
                     "splits": plan["splits"],
                     "cpu_oracle_interactions_per_s": cpu["value"], "cpu_cores": cpu["cores"],
                     "cpu_oracle_1thread_interactions_per_s": cpu1["value"] if cpu1 else None})

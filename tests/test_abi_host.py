@@ -262,8 +262,8 @@ def test_auto_path_choice():
     assert apg.nbody_plan_forces(1024, 152)["path"] == apg.NBODY_PATH_CLUSTER
     assert apg.nbody_plan_forces(4096, 152)["path"] == apg.NBODY_PATH_CLUSTER
     assert apg.nbody_plan_forces(8192, 152)["path"] == apg.NBODY_PATH_TILED
-    assert apg.nbody_plan_forces(32767, 152)["path"] == apg.NBODY_PATH_TILED
-    assert apg.nbody_plan_forces(32768, 152)["path"] == apg.NBODY_PATH_SYMMETRIC
+    assert apg.nbody_plan_forces(24575, 152)["path"] == apg.NBODY_PATH_TILED
+    assert apg.nbody_plan_forces(24576, 152)["path"] == apg.NBODY_PATH_SYMMETRIC
     assert apg.nbody_plan_forces(1048576, 152)["path"] == apg.NBODY_PATH_SYMMETRIC
     with pytest.raises(apg.NbodyError):
         apg.nbody_plan_forces(1000, 152, path=apg.NBODY_PATH_CLUSTER, splits=3)
