@@ -300,7 +300,9 @@ __global__ void reduce_sym_kernel(const float4 *__restrict__ ipart, int splits,
 // and dropped: two partners per step side by side (K = 4, 6, 8: 1-9 %
 // slower), 1/d^2 from a MUFU reciprocal instead of a packed multiply (one
 // FMA-pipe operation fewer per pair, 2.5 % slower), 3 CTAs per SM at K = 4
-// (12 % slower), 32-body units (1-3 % slower).
+// (12 % slower), 32-body units (1-3 % slower), the next step's source
+// shuffled one step ahead (1.5 % slower), the i-side folded every 64
+// sources instead of 32 (1.2 % slower).
 #define NBODY_SYM_LIST(X)                 \
     X(8, 8, 64, 2, 2)    /* 0: default */ \
     X(8, 8, 128, 2, 2)   /* 1 */          \

@@ -36,6 +36,7 @@ FP32_LANES_PER_SM_CLK = 128
 RECIPE_SM_MAX_MHZ = 2070.0    # fallback if no measured peaks file is present
 PATH_SYMMETRIC = 3
 PATH_NAMES = {1: "tiled", 2: "cluster", 3: "symmetric"}
+PATH_IDS = {"auto": 0, "tiled": 1, "symmetric": 3}
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the force kernel at N = 2^20, from one ncu capture, keyed by a hash of the
@@ -47,7 +48,7 @@ KERNEL_SOURCES = {
                   "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"],
 }
 TRAFFIC_BY_SOURCE = {
-    "b76a733875a3fee3": {"bytes": 419.60e6 + 4.56e9,
+    "ddf7f8efdc214481": {"bytes": 419.60e6 + 4.56e9,
                          "profile": "profiles/forces_sym_plummer1048576_dram.md"},
 }
 
@@ -59,6 +60,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="plummer1048576")
+    ap.add_argument("--path", choices=["auto", "tiled", "symmetric"], default="auto",
+                    help="force path of the timed step and e2e (auto: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-small-n", action="store_true",
@@ -71,11 +74,17 @@ def parse():
 
 
 def kernel_source_hash(kind):
+    """Hash of the kernel's source files with comments and blank space
+    removed: a change of code changes it, a change of comments does not."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
@@ -355,7 +364,8 @@ def run_ours(args):
     w = W.named(args.config)
     n = w.n
     pairs = float(n) * float(n)
-    plan = apg.nbody_plan_forces(n, props.multi_processor_count)
+    path = PATH_IDS[args.path]
+    plan = apg.nbody_plan_forces(n, props.multi_processor_count, path=path)
     launches_per_step = (2 if plan["scratch_bytes"] > 0 else 1) + 1
 
     pm0 = torch.from_numpy(w.pos_mass).to(device)
@@ -368,7 +378,7 @@ def run_ours(args):
     eps2, dt = float(w.eps2), float(w.dt)
 
     def step():
-        apg.nbody_forces(pm, eps2, acc)
+        apg.nbody_forces_ex(pm, eps2, acc, path=path)
         apg.nbody_euler_step(pm, vel, acc, dt)
 
     for _ in range(args.warmup):
@@ -385,7 +395,7 @@ def run_ours(args):
         for k in range(args.steps):
             flush.zero_()
             ev[k][0].record(stream)
-            apg.nbody_forces(pm, eps2, acc)
+            apg.nbody_forces_ex(pm, eps2, acc, path=path)
             ev[k][1].record(stream)
             apg.nbody_euler_step(pm, vel, acc, dt)
             ev[k][2].record(stream)
@@ -411,7 +421,7 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(apg, w, device, args.steps, world)
+        e2e = run_e2e(apg, w, device, args.steps, world, path)
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -439,6 +449,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": w.name, "n": n, "eps2": eps2, "dt": dt,
                    "step": "nbody_forces (a + p) then nbody_euler_step",
+                   "path": args.path,
                    "l2": "flushed (256 MiB write) before each timed step, outside its events",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "plan": {k: plan[k] for k in ("path", "variant", "i_per_thread", "threads",
@@ -487,7 +498,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(apg, w, device, steps, world):
+def run_e2e(apg, w, device, steps, world, path=0):
     """Same metric through the C ABI from host buffers: per step, copy the
     bodies and velocities in from pinned memory, compute, copy the new state
     and the accelerations/potentials back."""
@@ -505,7 +516,7 @@ def run_e2e(apg, w, device, steps, world):
     def one():
         d_pm.copy_(h_pm, non_blocking=True)
         d_vel.copy_(h_vel, non_blocking=True)
-        apg.nbody_forces(d_pm, eps2, d_acc)
+        apg.nbody_forces_ex(d_pm, eps2, d_acc, path=path)
         apg.nbody_euler_step(d_pm, d_vel, d_acc, dt)
         h_out[0].copy_(d_pm, non_blocking=True)
         h_out[1].copy_(d_vel, non_blocking=True)
