@@ -335,6 +335,7 @@ def test_symmetric_path_counts_every_pair_once(n, splits):
     one = gpu_forces(np.array([[0.5, 0.5, 0.5, 1.0]], np.float32), 2.0 ** 40, path=SYM)
     t = -float(one[0, 3])
     assert abs(t * 2.0 ** 20 - 1.0) < 2.0 ** -21
+    print(f"potential term t = 2^-20 * {t * 2.0 ** 20!r} (exact count: {t == 2.0 ** -20})")
     pm = np.zeros((n, 4), np.float32)
     pm[:, :3] = W.Stream(n).uniform(3 * n, -1.0, 1.0).reshape(n, 3)
     pm[:, 3] = 1.0
@@ -345,6 +346,19 @@ def test_symmetric_path_counts_every_pair_once(n, splits):
         assert np.array_equal(count, np.full(n, float(n))), (count.min(), count.max())
     else:   # fp32 sums of an inexact t: rounding well below one count
         assert np.abs(count - n).max() < 0.25, (count.min(), count.max())
+
+
+@pytest.mark.slow
+def test_symmetric_path_partials_past_2_34_bytes():
+    """n = 2^21 + 7: 1025 blocks (odd) with a ragged last one, and 512 j-side
+    slots of n records: about 17 GB of partials, so their byte offsets pass
+    2^34; every body must have met every body exactly once."""
+    n = 2 ** 21 + 7
+    plan = apg.nbody_plan_forces(n, torch.cuda.get_device_properties(0).multi_processor_count,
+                                 path=SYM)
+    assert plan["num_iblocks"] == 1025 and plan["scratch_bytes"] == 16 * (plan["splits"] + 512) * n
+    assert plan["scratch_bytes"] > 2 ** 34
+    test_symmetric_path_counts_every_pair_once(n, 0)
 
 
 def test_symmetric_path_deterministic_and_ts_identical():
