@@ -68,7 +68,7 @@ __device__ __forceinline__ float4 body_or_zero(const float4 *__restrict__ bodies
 // One chunk both ways: the lane's targets against the 32 home sources of the
 // warp, i-side into (ax, ay, az, pp), j-side returned for this lane's home
 // source as (ax, ay, az, -p).
-template <int KP, int U>
+template <int KP, int U, bool GF>
 __device__ __forceinline__ float4 chunk_sym(float4 home, const f2 (&xi)[KP], const f2 (&yi)[KP],
                                             const f2 (&zi)[KP], const f2 (&nmi)[KP], f2 e2,
                                             f2 (&ax)[KP], f2 (&ay)[KP], f2 (&az)[KP],
@@ -82,9 +82,14 @@ __device__ __forceinline__ float4 chunk_sym(float4 home, const f2 (&xi)[KP], con
         const float mj = __shfl_xor_sync(0xffffffffu, home.w, s);
         const Src sj = {f2_pack(xj, xj), f2_pack(yj, yj), f2_pack(zj, zj), f2_pack(mj, mj)};
         f2 tx = 0ull, ty = 0ull, tz = 0ull, tp = 0ull;
+        Geom gq[KP];
+        if constexpr (GF) {   // every pair's geometry and rsqrt before any accumulation
+#pragma unroll
+            for (int q = 0; q < KP; ++q) gq[q] = pair_geom(sj, xi[q], yi[q], zi[q], e2);
+        }
 #pragma unroll
         for (int q = 0; q < KP; ++q) {
-            const Geom g = pair_geom(sj, xi[q], yi[q], zi[q], e2);
+            const Geom g = GF ? gq[q] : pair_geom(sj, xi[q], yi[q], zi[q], e2);
             const f2 inv2 = f2_mul(g.inv, g.inv);
             const f2 inv3 = f2_mul(inv2, g.inv);          // 1 / d^3
             const f2 sc = f2_mul(sj.m, inv3);             // m_j / d^3
@@ -132,7 +137,7 @@ __device__ __forceinline__ void chunk_diag(float4 home, const f2 (&xi)[KP], cons
     }
 }
 
-template <int K, int W, int SUB, int MINB, int U>
+template <int K, int W, int SUB, int MINB, int U, bool GF>
 __global__ void __launch_bounds__(W * 32, MINB)
 forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, int splits,
                   float4 *__restrict__ ipart, float4 *__restrict__ jpart) {
@@ -201,7 +206,7 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
             if (k + 1 < nchunks) next = body_or_zero(bodies, home_index(k + 1), n);
             if (d != 0) {
                 jacc[buf][warp][c * 32 + lane] =
-                    chunk_sym<KP, U>(home, xi, yi, zi, nmi, e2, ax, ay, az, pp);
+                    chunk_sym<KP, U, GF>(home, xi, yi, zi, nmi, e2, ax, ay, az, pp);
             } else {
                 chunk_diag<KP, U>(home, xi, yi, zi, e2, ax, ay, az, pp);
             }
@@ -293,34 +298,41 @@ __global__ void reduce_sym_kernel(const float4 *__restrict__ ipart, int splits,
 }
 
 // Instantiated shapes: K targets per lane, W warps per CTA, SUB sources per
-// unit, the minimum resident CTAs per SM asked of the register allocator, and
-// the unroll factor of the 32-step chunk loop.  Variant 0 is the default, the
-// fastest measured on GB300 from N = 65536 to 2^20 (3.23e12 interactions/s at
-// 2^20; FMA pipe about 75 % busy, 125 registers, 2 CTAs per SM).  Measured
-// and dropped: two partners per step side by side (K = 4, 6, 8: 1-9 %
-// slower), 1/d^2 from a MUFU reciprocal instead of a packed multiply (one
-// FMA-pipe operation fewer per pair, 2.5 % slower), 3 CTAs per SM at K = 4
-// (12 % slower), 32-body units (1-3 % slower), the next step's source
-// shuffled one step ahead (1.5 % slower), the i-side folded every 64
-// sources instead of 32 (1.2 % slower).
-#define NBODY_SYM_LIST(X)                 \
-    X(8, 8, 64, 2, 2)    /* 0: default */ \
-    X(8, 8, 128, 2, 2)   /* 1 */          \
-    X(8, 4, 128, 4, 2)   /* 2 */          \
-    X(6, 8, 64, 2, 2)    /* 3 */          \
-    X(4, 8, 64, 2, 2)    /* 4 */
+// unit, the minimum resident CTAs per SM asked of the register allocator, the
+// unroll factor of the 32-step chunk loop, and GF: the geometry and rsqrt of
+// all K/2 target pairs computed before any of their accumulations (the
+// rsqrt latencies overlap).  Variant 0 is the default, the fastest measured
+// on GB300 from N = 65536 to 2^20 (3.31e12 interactions/s at 2^20; 118
+// registers, 2 CTAs per SM).  Measured and dropped, each relative to the
+// best shape of its time:
+//   128-body units (1.5-2.5 % slower), 32-body units (2-3 % slower);
+//   K = 6 or 4 (6-12 % slower); W = 4 with 4 CTAs per SM (+0.3 % at 2^20,
+//   10 % slower at 200003 bodies);
+//   the chunk loop unrolled by 2 or 4 (2-4 % slower);
+//   two partners per step side by side (1-9 % slower);
+//   1/d^2 from a MUFU reciprocal instead of a packed multiply, one FMA-pipe
+//   operation fewer per pair (2.5 % slower);
+//   the next step's partner shuffled a step ahead (1.5-5 % slower);
+//   the i-side folded every 64 sources instead of 32 (1.2 % slower);
+//   3 CTAs per SM at K = 4 (12 % slower).
+#define NBODY_SYM_LIST(X)                     \
+    X(8, 8, 64, 2, 1, true)   /* 0: default */ \
+    X(8, 8, 64, 2, 2, false)  /* 1 */          \
+    X(8, 4, 64, 4, 1, true)   /* 2 */          \
+    X(6, 8, 64, 2, 1, true)   /* 3 */          \
+    X(4, 8, 64, 2, 1, true)   /* 4 */
 
-#define NBODY_SYM_ENTRY(K, W, SUB, MINB, U)                                  \
+#define NBODY_SYM_ENTRY(K, W, SUB, MINB, U, GF)                                  \
     {K, W, SUB, MINB, SymShape<K, W, SUB>::smem_bytes,                             \
-     reinterpret_cast<const void *>(&forces_sym_kernel<K, W, SUB, MINB, U>)},
+     reinterpret_cast<const void *>(&forces_sym_kernel<K, W, SUB, MINB, U, GF>)},
 
 const SymVariant kSymVariants[] = {NBODY_SYM_LIST(NBODY_SYM_ENTRY)};
 
-template <int K, int W, int SUB, int MINB, int U>
+template <int K, int W, int SUB, int MINB, int U, bool GF>
 cudaError_t launch_sym_variant(const float *bodies, int n, float eps2, int nb, int splits,
                                float4 *ipart, float4 *jpart, cudaStream_t stream) {
     const unsigned grid = static_cast<unsigned>(nb) * static_cast<unsigned>(splits);
-    forces_sym_kernel<K, W, SUB, MINB, U>
+    forces_sym_kernel<K, W, SUB, MINB, U, GF>
         <<<grid, W * 32, SymShape<K, W, SUB>::smem_bytes, stream>>>(
             reinterpret_cast<const float4 *>(bodies), n, eps2, nb, splits, ipart, jpart);
     return cudaGetLastError();
@@ -329,7 +341,7 @@ cudaError_t launch_sym_variant(const float *bodies, int n, float eps2, int nb, i
 typedef cudaError_t (*SymLauncher)(const float *, int, float, int, int, float4 *, float4 *,
                                    cudaStream_t);
 
-#define NBODY_SYM_LAUNCHER(K, W, SUB, MINB, U) &launch_sym_variant<K, W, SUB, MINB, U>,
+#define NBODY_SYM_LAUNCHER(K, W, SUB, MINB, U, GF) &launch_sym_variant<K, W, SUB, MINB, U, GF>,
 
 const SymLauncher kSymLaunchers[] = {NBODY_SYM_LIST(NBODY_SYM_LAUNCHER)};
 

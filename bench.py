@@ -48,7 +48,7 @@ KERNEL_SOURCES = {
                   "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"],
 }
 TRAFFIC_BY_SOURCE = {
-    "ddf7f8efdc214481": {"bytes": 419.60e6 + 4.56e9,
+    "120d3b6331161c56": {"bytes": 391.38e6 + 4.56e9,
                          "profile": "profiles/forces_sym_plummer1048576_dram.md"},
 }
 
