@@ -301,13 +301,15 @@ __global__ void reduce_sym_kernel(const float4 *__restrict__ ipart, int splits,
 // unit, the minimum resident CTAs per SM asked of the register allocator, the
 // unroll factor of the 32-step chunk loop, and GF: the geometry and rsqrt of
 // all K/2 target pairs computed before any of their accumulations (the
-// rsqrt latencies overlap).  Variant 0 is the default, the fastest measured
-// on GB300 from N = 65536 to 2^20 (3.31e12 interactions/s at 2^20; 118
-// registers, 2 CTAs per SM).  Measured and dropped, each relative to the
-// best shape of its time:
+// rsqrt latencies overlap).  Variants 0-2 differ only in the block size (W =
+// 8, 4, 2 warps: 2048, 1024, 512 bodies); the planner takes the smaller
+// blocks for smaller n, whose waves they fill better, and variant 0 from
+// about 160K bodies, where fewer partial slots win (3.31e12 interactions/s at
+// 2^20; 118 registers).  Variants 3-5 stay selectable for tests and sweeps.
+// Measured and dropped, each relative to the best shape of its time:
 //   128-body units (1.5-2.5 % slower), 32-body units (2-3 % slower);
-//   K = 6 or 4 (6-12 % slower); W = 4 with 4 CTAs per SM (+0.3 % at 2^20,
-//   10 % slower at 200003 bodies);
+//   K = 6 or 4 (6-12 % slower); K = 2 or 4 with 32-body units and 256- or
+//   512-body blocks (slower than variant 2 at every size from 2048 bodies);
 //   the chunk loop unrolled by 2 or 4 (2-4 % slower);
 //   two partners per step side by side (1-9 % slower);
 //   1/d^2 from a MUFU reciprocal instead of a packed multiply, one FMA-pipe
@@ -317,10 +319,11 @@ __global__ void reduce_sym_kernel(const float4 *__restrict__ ipart, int splits,
 //   3 CTAs per SM at K = 4 (12 % slower).
 #define NBODY_SYM_LIST(X)                     \
     X(8, 8, 64, 2, 1, true)   /* 0: default */ \
-    X(8, 8, 64, 2, 2, false)  /* 1 */          \
-    X(8, 4, 64, 4, 1, true)   /* 2 */          \
-    X(6, 8, 64, 2, 1, true)   /* 3 */          \
-    X(4, 8, 64, 2, 1, true)   /* 4 */
+    X(8, 4, 64, 4, 1, true)   /* 1 */          \
+    X(8, 2, 64, 8, 1, true)   /* 2 */          \
+    X(8, 8, 64, 2, 2, false)  /* 3 */          \
+    X(6, 8, 64, 2, 1, true)   /* 4 */          \
+    X(4, 8, 64, 2, 1, true)   /* 5 */
 
 #define NBODY_SYM_ENTRY(K, W, SUB, MINB, U, GF)                                  \
     {K, W, SUB, MINB, SymShape<K, W, SUB>::smem_bytes,                             \

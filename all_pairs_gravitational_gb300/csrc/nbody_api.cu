@@ -259,12 +259,20 @@ void plan_cluster_variant(int64_t nt, int64_t ns, int sm, int occ, int variant, 
 constexpr int64_t kClusterMaxN = 6144;
 
 // Symmetric path (each unordered pair once).  Smallest n the automatic choice
-// sends to it (measured on GB300: 2.48e12 against the tiled path's 2.25e12
-// interactions/s at 24576 bodies, 1.90e12 against 2.15e12 at 16384), its
-// default variant, and the cap on its partials: the j-side partials take
-// (nb - 1) / 2 (+1) records per body, so they grow as n^2 / T.
-constexpr int64_t kSymMinN = 24576;
-constexpr int kDefaultSymVariant = 0;
+// sends to it, and the variant it takes by size, measured on GB300 inside
+// CUDA graphs: from 10240 bodies every shape below beats the tiled path
+// (54.5 against 57.6 us at 10240; 221 against 264 us at 24576), 512-body
+// blocks win up to about 45K bodies (better filled waves), 1024-body blocks
+// up to about 160K, and 2048-body blocks above (fewer partial slots); each
+// choice is within 4.5 % of the fastest shape at every size measured.  The
+// j-side partials take (nb - 1) / 2 (+1) records per body, so they grow as
+// n^2 / T: the cap below bounds them.
+constexpr int64_t kSymMinN = 10240;
+constexpr int64_t kSymMidN = 45056;     // from here 1024-body blocks
+constexpr int64_t kSymLargeN = 163840;  // from here 2048-body blocks
+constexpr int kSymSmallVariant = 2;     // K = 8, 2 warps: 512-body blocks
+constexpr int kSymMidVariant = 1;       // K = 8, 4 warps: 1024-body blocks
+constexpr int kDefaultSymVariant = 0;   // K = 8, 8 warps: 2048-body blocks
 constexpr int64_t kMaxSymScratchBytes = int64_t(24) << 30;
 // Relative cost model of the symmetric path: evaluations (two interactions
 // each) per SM-second, the fixed cost of a CTA in evaluations, scratch traffic.
@@ -338,6 +346,10 @@ bool plan_sym(int64_t n, int sm, int occ, int variant, int splits_req, nbody_pla
     return true;
 }
 
+int auto_sym_variant(int64_t n) {
+    return n < kSymMidN ? kSymSmallVariant : (n < kSymLargeN ? kSymMidVariant : kDefaultSymVariant);
+}
+
 // all_pairs: the targets are the sources (same array, nt == ns), the case the
 // symmetric path needs.
 nbody_status make_plan(int64_t nt, int64_t ns, bool all_pairs, int sm, const Occupancy &occ,
@@ -363,14 +375,15 @@ nbody_status make_plan(int64_t nt, int64_t ns, bool all_pairs, int sm, const Occ
         if (nt <= kClusterMaxN && ns <= kClusterMaxN) {
             path = NBODY_PATH_CLUSTER;
         } else if (all_pairs && nt >= kSymMinN &&
-                   plan_sym(nt, sm, occ.sym[kDefaultSymVariant], kDefaultSymVariant, o.splits, p)) {
+                   plan_sym(nt, sm, occ.sym[auto_sym_variant(nt)], auto_sym_variant(nt), o.splits,
+                            p)) {
             return NBODY_OK;
         } else {
             path = NBODY_PATH_TILED;
         }
     }
     if (path == NBODY_PATH_SYMMETRIC) {
-        const int variant = o.variant < 0 ? kDefaultSymVariant : o.variant;
+        const int variant = o.variant < 0 ? auto_sym_variant(nt) : o.variant;
         if (variant >= nbody::sym_variant_count() || variant >= kMaxVariants)
             return NBODY_ERR_INVALID_ARG;
         return plan_sym(nt, sm, occ.sym[variant], variant, o.splits, p) ? NBODY_OK

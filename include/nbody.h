@@ -66,7 +66,7 @@ typedef enum nbody_status {
  * same n, inputs and GPU model.  Large n may split the source range over
  * CTAs and add the fp32 partials in a fixed order in a second kernel; the
  * partials live in stream-ordered memory from a library-owned pool.  From
- * n = 24576 each unordered pair is evaluated once for both bodies (the
+ * n = 10240 each unordered pair is evaluated once for both bodies (the
  * symmetric path below).
  *
  * Errors: NBODY_ERR_INVALID_ARG, _MISALIGNED, _ALIAS (host checks, nothing
@@ -166,7 +166,8 @@ enum {
  * bit-reproducible.  It needs targets == sources (nbody_forces, or
  * nbody_forces_ts with the same array and nt == ns), default precision, and
  * partials within 24 GiB (n up to about 2.5 million); automatic planning uses
- * it for n >= 24576 when those hold.
+ * it for n >= 10240 when those hold, with blocks of 512, 1024 or 2048 bodies
+ * as n grows.
  */
 
 typedef struct nbody_forces_opts {

@@ -262,8 +262,12 @@ def test_auto_path_choice():
     assert apg.nbody_plan_forces(1024, 152)["path"] == apg.NBODY_PATH_CLUSTER
     assert apg.nbody_plan_forces(4096, 152)["path"] == apg.NBODY_PATH_CLUSTER
     assert apg.nbody_plan_forces(8192, 152)["path"] == apg.NBODY_PATH_TILED
-    assert apg.nbody_plan_forces(24575, 152)["path"] == apg.NBODY_PATH_TILED
-    assert apg.nbody_plan_forces(24576, 152)["path"] == apg.NBODY_PATH_SYMMETRIC
+    assert apg.nbody_plan_forces(10239, 152)["path"] == apg.NBODY_PATH_TILED
+    assert apg.nbody_plan_forces(10240, 152)["path"] == apg.NBODY_PATH_SYMMETRIC
+    # the symmetric block size grows with n: 512, 1024, then 2048 bodies
+    blocks = [apg.nbody_plan_forces(n, 152)["threads"] * apg.nbody_plan_forces(n, 152)["i_per_thread"]
+              for n in (10240, 45055, 45056, 163839, 163840, 1048576)]
+    assert blocks == [512, 512, 1024, 1024, 2048, 2048]
     assert apg.nbody_plan_forces(1048576, 152)["path"] == apg.NBODY_PATH_SYMMETRIC
     with pytest.raises(apg.NbodyError):
         apg.nbody_plan_forces(1000, 152, path=apg.NBODY_PATH_CLUSTER, splits=3)
