@@ -125,6 +125,17 @@ def test_clumps200003_sampled():
     assert_parity(acc, oracle.forces(w.pos_mass, w.eps2, rows=rows), rows)
 
 
+@pytest.mark.parametrize("name", ["clumps200003", "plummer65536"])
+def test_tiled_path_at_large_n(name):
+    """The ordered-pair tiled kernel forced at sizes the automatic choice
+    sends to the symmetric path (it still serves the compensated precision,
+    the target/source form and n beyond the symmetric partials' cap)."""
+    w = W.named(name)
+    acc = gpu_forces(w.pos_mass, w.eps2, path=apg.NBODY_PATH_TILED)
+    rows = np.unique(np.concatenate([sample_rows(w.n, 1024, 6), np.arange(w.n - 100, w.n)]))
+    assert_parity(acc, oracle.forces(w.pos_mass, w.eps2, rows=rows), rows)
+
+
 @pytest.mark.slow
 def test_plummer1048576_sampled_in_bench_configuration():
     """The full-size workload in the launch configuration the benchmark times
@@ -449,9 +460,11 @@ def _separate_steps(w, steps):
 
 
 @pytest.mark.parametrize("name,steps", [("smallcube1024", 20), ("smallcube1024", 7),
-                                        ("smallcube4096", 3), ("plummer65536", 10),
-                                        ("clumps200003", 2)])
+                                        ("smallcube4096", 3), ("smallcube8192", 4),
+                                        ("plummer65536", 10), ("clumps200003", 2)])
 def test_simulate_is_the_separate_calls(name, steps):
+    """Cluster path (fused pairs of steps), tiled path (8192) and symmetric
+    path (65536, 200003)."""
     w = W.named(name)
     ref = _separate_steps(w, steps)
     pm = torch.from_numpy(w.pos_mass).to(dev())
