@@ -316,7 +316,12 @@ __global__ void reduce_sym_kernel(const float4 *__restrict__ ipart, int splits,
 //   operation fewer per pair (2.5 % slower);
 //   the next step's partner shuffled a step ahead (1.5-5 % slower);
 //   the i-side folded every 64 sources instead of 32 (1.2 % slower);
-//   3 CTAs per SM at K = 4 (12 % slower).
+//   3 CTAs per SM at K = 4 (12 % slower);
+//   each unit's cross-warp j-side sums spread over all threads, one component
+//   each, instead of one thread per source (1.2 % slower);
+//   the potential terms or the j-side sums as scalar fp32 FMAs (6-10 %
+//   slower: packed f32x2 instructions occupy both halves of the FMA pipe, so
+//   no half is left idle for scalar work).
 #define NBODY_SYM_LIST(X)                     \
     X(8, 8, 64, 2, 1, true)   /* 0: default */ \
     X(8, 4, 64, 4, 1, true)   /* 1 */          \
