@@ -310,9 +310,10 @@ bool plan_sym(int64_t n, int sm, int occ, int variant, int splits_req, nbody_pla
     const double slot_rate = kSymEvalsPerSmSecond / (occ > 0 ? occ : 1);
     const double unit_evals = static_cast<double>(g.block) * v.sub;
 
-    int64_t s_lo = 1, s_hi = std::min<int64_t>(g.units, kMaxSplits);
-    s_hi = std::max<int64_t>(1, std::min<int64_t>(s_hi, (kMaxSymScratchBytes - jbytes) / (16 * n)));
-    if (splits_req > 0) s_lo = s_hi = std::min<int64_t>(splits_req, g.units);
+    // pieces allowed by the partials' cap (each piece adds one i-side slot)
+    const int64_t s_cap = std::max<int64_t>(1, (kMaxSymScratchBytes - jbytes) / (16 * n));
+    int64_t s_lo = 1, s_hi = std::min<int64_t>(std::min<int64_t>(g.units, kMaxSplits), s_cap);
+    if (splits_req > 0) s_lo = s_hi = std::min<int64_t>(std::min<int64_t>(splits_req, g.units), s_cap);
 
     double best_t = INFINITY;
     int64_t best_s = 1, best_upp = g.units, best_waves = 1;

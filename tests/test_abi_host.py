@@ -220,6 +220,12 @@ def test_symmetric_plan(lib, n, splits):
         assert plan["splits"] == min(splits, units) or plan["splits"] == splits
 
 
+def test_symmetric_plan_forced_splits_stay_within_the_cap():
+    plan = apg.nbody_plan_forces(2 ** 21, 152, path=apg.NBODY_PATH_SYMMETRIC, splits=1000)
+    assert plan["scratch_bytes"] <= 24 << 30 and plan["splits"] < 1000
+    _sym_covers(plan, 2 ** 21)
+
+
 def test_symmetric_plan_limits():
     with pytest.raises(apg.NbodyError):      # j-side partials beyond 24 GiB
         apg.nbody_plan_forces(2 ** 23, 152, path=apg.NBODY_PATH_SYMMETRIC)
