@@ -55,6 +55,9 @@ def _load():
                                              ctypes.c_int64, ctypes.c_float, ctypes.c_void_p,
                                              ctypes.c_int]
             lib.oracle_forces_ts.restype = ctypes.c_int
+            lib.oracle_forces_f64.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_double,
+                                              ctypes.c_void_p, ctypes.c_int]
+            lib.oracle_forces_f64.restype = ctypes.c_int
             lib.oracle_euler.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_int64, ctypes.c_float]
             lib.oracle_euler.restype = ctypes.c_int
@@ -112,4 +115,32 @@ def euler(pos_mass, vel, acc_pot, dt):
                           ctypes.c_float(np.float32(dt)))
     if rc != 0:
         raise ValueError("oracle_euler rejected its arguments")
+    return pm, v
+
+
+def forces_f64(bodies, eps2, threads: int = 0) -> np.ndarray:
+    """All-pairs (ax, ay, az, p) of fp64 bodies [n, 4] (x, y, z, m), in fp64."""
+    lib = _load()
+    b = np.ascontiguousarray(bodies, dtype=np.float64)
+    if b.ndim != 2 or b.shape[1] != 4:
+        raise ValueError(f"expected an [n, 4] array, got shape {b.shape}")
+    out = np.empty_like(b)
+    rc = lib.oracle_forces_f64(b.ctypes.data, b.shape[0], float(eps2), out.ctypes.data,
+                               int(threads))
+    if rc != 0:
+        raise ValueError("oracle_forces_f64 rejected its arguments")
+    return out
+
+
+def trajectory_f64(pos_mass, vel, eps2, dt, steps, threads: int = 0):
+    """`steps` explicit Euler steps kept in fp64 throughout (the lecture's order:
+    positions from the old velocities, then velocities from a); returns the
+    fp64 (pos_mass, vel) after the last step."""
+    pm = np.array(pos_mass, dtype=np.float64)
+    v = np.array(vel, dtype=np.float64)
+    dt = float(dt)
+    for _ in range(int(steps)):
+        a = forces_f64(pm, eps2, threads)
+        pm[:, :3] = pm[:, :3] + dt * v[:, :3]
+        v[:, :3] = v[:, :3] + dt * a[:, :3]
     return pm, v

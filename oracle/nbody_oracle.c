@@ -107,6 +107,54 @@ int oracle_forces_ts(const float *targets, int64_t nt,
 }
 
 /*
+ * The same definition with fp64 bodies: all-pairs over n bodies whose
+ * positions and masses are doubles, for the fp64 reference trajectory (an
+ * Euler integration kept in fp64 throughout).  On bodies that fp32 holds
+ * exactly it gives the same bits as oracle_forces_ts with targets ==
+ * sources, the same arithmetic in the same order.
+ *
+ *   bodies  : n bodies, 4 doubles each (x, y, z, m).
+ *   eps2    : the softening eps^2.
+ *   out     : n rows of 4 doubles (ax, ay, az, p).
+ *
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_forces_f64(const double *bodies, int64_t n, double eps2, double *out, int nthreads)
+{
+    if (n < 0) return -1;
+    if (n > 0 && (bodies == NULL || out == NULL)) return -1;
+#ifdef _OPENMP
+    int nth = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 8) num_threads(nth)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t i = 0; i < n; ++i) {
+        const double *b = bodies + 4 * i;
+        double sx = 0.0, sy = 0.0, sz = 0.0, pot = 0.0;
+        for (int64_t q = 0; q < n; ++q) {
+            const double *src = bodies + 4 * q;
+            const double dx = src[0] - b[0];
+            const double dy = src[1] - b[1];
+            const double dz = src[2] - b[2];
+            const double m = src[3];
+            const double dd = dx * dx + dy * dy + dz * dz + eps2;   /* |r|^2 + eps^2 */
+            const double w = 1.0 / sqrt(dd);
+            const double k = m * w * w * w;                        /* m (|r|^2 + eps^2)^(-3/2) */
+            sx += k * dx;
+            sy += k * dy;
+            sz += k * dz;
+            pot -= m * w;
+        }
+        out[4 * i + 0] = sx;
+        out[4 * i + 1] = sy;
+        out[4 * i + 2] = sz;
+        out[4 * i + 3] = pot;
+    }
+    return 0;
+}
+
+/*
  * Explicit Euler step in fp32, in place.
  *
  *   pos_mass: n bodies (x, y, z, m); x, y, z updated, m untouched.

@@ -306,3 +306,43 @@ def test_euler_velocity_uses_acceleration_and_keeps_w():
             exp = _rne_f32(Fraction(float(w.vel[i, c])) +
                            _rne_f32(Fraction(float(dt)) * Fraction(float(acc[i, c]))))
             assert Fraction(float(v2[i, c])) == exp
+
+
+# ---------------------------------------------------------------- fp64 trajectory
+
+def test_forces_f64_is_the_pinned_definition_on_fp32_bodies():
+    """On bodies fp32 holds exactly, the fp64-input entry point gives the bits
+    of the pinned fp32-input one: the same arithmetic in the same order."""
+    w = W.clumps(700, seed=31)
+    eps2 = np.float32(w.eps2)
+    got = oracle.forces_f64(w.pos_mass.astype(np.float64), float(eps2))
+    assert np.array_equal(got, oracle.forces(w.pos_mass, eps2))
+
+
+def test_trajectory_f64_free_body_moves_in_a_straight_line():
+    """A lone body feels no force (its own term adds 0 to a): with dt a power
+    of two and dyadic coordinates every fp64 step is exact."""
+    pm = np.array([[0.5, -0.25, 2.0, 3.0]])
+    v = np.array([[1.0, 0.5, -0.25, 0.0]])
+    dt = 2.0 ** -10
+    for k in (1, 7, 64):
+        pm_k, v_k = oracle.trajectory_f64(pm, v, 1e-4, dt, k)
+        assert np.array_equal(pm_k[:, :3], pm[:, :3] + k * dt * v[:, :3])
+        assert np.array_equal(v_k, v) and pm_k[0, 3] == 3.0
+
+
+def test_trajectory_f64_moves_positions_with_the_old_velocity():
+    """From rest, one step leaves the positions where they were (they move
+    with the velocity from before the step) and sets v = dt a; the next step
+    moves them by dt^2 a."""
+    pm = np.array([[0.0, 0.0, 0.0, 1.0], [3.0, 4.0, 0.0, 2.0]])
+    v = np.zeros((2, 4))
+    dt = 2.0 ** -4
+    a0 = oracle.forces_f64(pm, 144.0)
+    pm1, v1 = oracle.trajectory_f64(pm, v, 144.0, dt, 1)
+    assert np.array_equal(pm1, pm)
+    assert np.array_equal(v1[:, :3], dt * a0[:, :3])
+    pm2, _ = oracle.trajectory_f64(pm, v, 144.0, dt, 2)
+    assert np.array_equal(pm2[:, :3], pm[:, :3] + dt * (dt * a0[:, :3]))
+    # the worked two-body value (distance 5, eps 12: |r|^2 + eps^2 = 13^2)
+    assert a0[0, 0] == pytest.approx(2.0 * 3.0 / 13.0 ** 3, rel=1e-15)

@@ -116,6 +116,29 @@ def test_plummer65536_ten_steps():
         assert np.array_equal(vel.cpu().numpy(), v_ref), step
 
 
+@pytest.mark.slow
+def test_plummer65536_trajectory_against_fp64():
+    """The ten GPU steps of the Plummer workload against the same ten Euler
+    steps kept in fp64 throughout (the oracle's fp64 forces and fp64
+    updates): the fp32 trajectory drifts from it only by rounding."""
+    w = W.named("plummer65536")
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    vel = torch.from_numpy(w.vel).to(dev())
+    acc = torch.empty_like(pm)
+    apg.nbody_simulate(pm, vel, acc, float(w.eps2), float(w.dt), w.steps)
+    torch.cuda.synchronize()
+    pm64, v64 = oracle.trajectory_f64(w.pos_mass, w.vel, float(np.float32(w.eps2)),
+                                      float(np.float32(w.dt)), w.steps)
+    dx = np.abs(pm.cpu().numpy()[:, :3].astype(np.float64) - pm64[:, :3])
+    dv = np.abs(vel.cpu().numpy()[:, :3].astype(np.float64) - v64[:, :3])
+    rx = dx.max() / np.abs(pm64[:, :3]).max()
+    rv = dv.max() / np.abs(v64[:, :3]).max()
+    print(f"fp64 trajectory drift after {w.steps} steps: max |dx| {dx.max():.3e} "
+          f"(rms {np.sqrt((dx ** 2).mean()):.3e}), max |dv| {dv.max():.3e} "
+          f"(rms {np.sqrt((dv ** 2).mean()):.3e})")
+    assert rx < 1e-6 and rv < 1e-5, (rx, rv)
+
+
 def test_clumps200003_sampled():
     w = W.named("clumps200003")
     acc = gpu_forces(w.pos_mass, w.eps2)
