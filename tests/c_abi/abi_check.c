@@ -74,6 +74,30 @@ int main(void) {
     printf("nbody_forces from C: worst per-body relative error %.3e\n", worst);
     if (!(worst <= 1e-4)) return 5;
 
+    /* the symmetric path forced through the options struct, and the planner's
+     * automatic choice at 2^20 bodies, from C */
+    nbody_forces_opts opts = {NBODY_PATH_SYMMETRIC, -1, 0, NBODY_PRECISION_DEFAULT};
+    static float acc_sym[N * 4];
+    if ((st = nbody_forces_ex(d_pm, N, EPS2, d_vel, &opts, 0)) != NBODY_OK) return 10;
+    cudaMemcpy(acc_sym, d_vel, sizeof acc_sym, cudaMemcpyDeviceToHost);
+    cudaMemcpy(d_vel, vel, sizeof vel, cudaMemcpyHostToDevice);         /* restore */
+    double worst_sym = 0.0;
+    for (int i = 0; i < N; ++i) {
+        double d = 0, na = 0;
+        for (int c = 0; c < 3; ++c) {
+            d += (double)(acc_sym[4 * i + c] - acc[4 * i + c]) * (acc_sym[4 * i + c] - acc[4 * i + c]);
+            na += (double)acc[4 * i + c] * acc[4 * i + c];
+        }
+        const double e = sqrt(d / na);
+        if (e > worst_sym) worst_sym = e;
+    }
+    printf("symmetric path from C: worst per-body difference %.3e\n", worst_sym);
+    if (!(worst_sym <= 2e-4)) return 11;
+    nbody_plan plan;
+    nbody_forces_opts autoo = {NBODY_PATH_AUTO, -1, 0, NBODY_PRECISION_DEFAULT};
+    if (nbody_plan_forces(1 << 20, 152, 0, &autoo, &plan) != NBODY_OK) return 12;
+    if (plan.path != NBODY_PATH_SYMMETRIC || plan.scratch_bytes <= 0) return 13;
+
     /* one Euler step, then the same step through nbody_simulate on a copy */
     cudaMemcpy(pm2, d_pm, sizeof pm2, cudaMemcpyDeviceToHost);
     if ((st = nbody_euler_step(d_pm, d_vel, d_acc, N, 1e-3f, 0)) != NBODY_OK) return 6;
