@@ -220,6 +220,25 @@ def test_symmetric_plan(lib, n, splits):
         assert plan["splits"] == min(splits, units) or plan["splits"] == splits
 
 
+@pytest.mark.parametrize("sm", [1, 148, 160, 264])
+@pytest.mark.parametrize("n", [10240, 45056, 163840, 1048576, 2097159])
+@pytest.mark.parametrize("variant", [-1, 0, 1, 2, 3, 4, 5])
+def test_symmetric_plan_other_gpus_and_variants(n, sm, variant):
+    ref = apg.nbody_plan_forces(4096, 152, path=apg.NBODY_PATH_SYMMETRIC, variant=variant)
+    t = ref["threads"] * ref["i_per_thread"]
+    nb = -(-n // t)
+    jslots = (nb - 1) // 2 + (1 if nb % 2 == 0 else 0)
+    if variant >= 0 and 16 * (jslots + 1) * n > 24 << 30:   # partials beyond the cap
+        with pytest.raises(apg.NbodyError):
+            apg.nbody_plan_forces(n, sm, path=apg.NBODY_PATH_SYMMETRIC, variant=variant)
+        return
+    plan = apg.nbody_plan_forces(n, sm, path=apg.NBODY_PATH_SYMMETRIC, variant=variant)
+    assert plan["path"] == apg.NBODY_PATH_SYMMETRIC
+    if variant >= 0:
+        assert plan["variant"] == variant
+    _sym_covers(plan, n)
+
+
 def test_symmetric_plan_forced_splits_stay_within_the_cap():
     plan = apg.nbody_plan_forces(2 ** 21, 152, path=apg.NBODY_PATH_SYMMETRIC, splits=1000)
     assert plan["scratch_bytes"] <= 24 << 30 and plan["splits"] < 1000
