@@ -12,6 +12,7 @@
 // stream HBM.
 #include <algorithm>
 
+#include "nbody_device.cuh"
 #include "nbody_internal.h"
 
 namespace nbody {
@@ -26,13 +27,7 @@ euler_kernel(float4 *__restrict__ pm, float4 *__restrict__ vel,
          i += stride) {
         float4 p = pm[i];
         float4 v = vel[i];
-        const float4 a = __ldg(acc + i);
-        p.x = __fadd_rn(p.x, __fmul_rn(dt, v.x));
-        p.y = __fadd_rn(p.y, __fmul_rn(dt, v.y));
-        p.z = __fadd_rn(p.z, __fmul_rn(dt, v.z));
-        v.x = __fadd_rn(v.x, __fmul_rn(dt, a.x));
-        v.y = __fadd_rn(v.y, __fmul_rn(dt, a.y));
-        v.z = __fadd_rn(v.z, __fmul_rn(dt, a.z));
+        euler_body(p, v, __ldg(acc + i), dt);
         pm[i] = p;
         vel[i] = v;
     }

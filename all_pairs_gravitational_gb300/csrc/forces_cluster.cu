@@ -182,12 +182,7 @@ __device__ __forceinline__ void reduce_and_store(WarpAcc<K / 2> &acc, float4 (*r
             if (EULER) {   // the step of euler.cu, on this body, positions first
                 float4 x = __ldg(reinterpret_cast<const float4 *>(pr.targets) + i);
                 float4 v = eu.vel[i];
-                x.x = __fadd_rn(x.x, __fmul_rn(eu.dt, v.x));
-                x.y = __fadd_rn(x.y, __fmul_rn(eu.dt, v.y));
-                x.z = __fadd_rn(x.z, __fmul_rn(eu.dt, v.z));
-                v.x = __fadd_rn(v.x, __fmul_rn(eu.dt, a.x));
-                v.y = __fadd_rn(v.y, __fmul_rn(eu.dt, a.y));
-                v.z = __fadd_rn(v.z, __fmul_rn(eu.dt, a.z));
+                euler_body(x, v, a, eu.dt);
                 eu.pos_out[i] = x;
                 eu.vel[i] = v;
             }

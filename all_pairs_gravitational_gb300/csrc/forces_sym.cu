@@ -266,10 +266,12 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
 
 // out[i] = the S i-side slots of body i, then its j-side slots (H of them,
 // H + 1 for a body of block >= nb / 2 when nb is even), added in that fixed
-// order with compensation.
+// order with compensation.  With EULER, the body's Euler step follows in
+// place (the force kernel has finished reading the positions).
+template <bool EULER>
 __global__ void reduce_sym_kernel(const float4 *__restrict__ ipart, int splits,
                                   const float4 *__restrict__ jpart, int n, int block, int nb,
-                                  float4 *__restrict__ out) {
+                                  float4 *__restrict__ out, EulerFuse eu) {
     const int H = (nb - 1) / 2;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
@@ -292,8 +294,16 @@ __global__ void reduce_sym_kernel(const float4 *__restrict__ ipart, int splits,
             kahan1(hz, cz, v.z);
             kahan1(hw, cw, v.w);
         }
-        out[i] = make_float4(__fsub_rn(hx, cx), __fsub_rn(hy, cy), __fsub_rn(hz, cz),
-                             __fsub_rn(hw, cw));
+        const float4 a = make_float4(__fsub_rn(hx, cx), __fsub_rn(hy, cy), __fsub_rn(hz, cz),
+                                     __fsub_rn(hw, cw));
+        out[i] = a;
+        if (EULER) {
+            float4 x = eu.pos_out[i];
+            float4 v = eu.vel[i];
+            euler_body(x, v, a, eu.dt);
+            eu.pos_out[i] = x;
+            eu.vel[i] = v;
+        }
     }
 }
 
@@ -369,11 +379,17 @@ cudaError_t launch_sym(int variant, const float *bodies, int n, float eps2, int 
 }
 
 cudaError_t launch_reduce_sym(const float4 *ipart, int splits, const float4 *jpart, int n,
-                              int block, int nb, float4 *out, int sm_count, cudaStream_t stream) {
+                              int block, int nb, float4 *out, int sm_count, cudaStream_t stream,
+                              const EulerFuse *euler) {
     const int threads = 256;
     const int64_t want = (static_cast<int64_t>(n) + threads - 1) / threads;
     const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sm_count) * 8));
-    reduce_sym_kernel<<<grid, threads, 0, stream>>>(ipart, splits, jpart, n, block, nb, out);
+    if (euler != nullptr)
+        reduce_sym_kernel<true><<<grid, threads, 0, stream>>>(ipart, splits, jpart, n, block, nb,
+                                                              out, *euler);
+    else
+        reduce_sym_kernel<false><<<grid, threads, 0, stream>>>(ipart, splits, jpart, n, block, nb,
+                                                               out, EulerFuse{nullptr, nullptr, 0.f});
     return cudaGetLastError();
 }
 

@@ -186,9 +186,12 @@ forces_tiled_kernel(const Problem pr, int num_ib, int tiles_per_split, int ntile
     }
 }
 
-// Fixed-order compensated sum of the S partials of each body.
+// Fixed-order compensated sum of the S partials of each body; with EULER,
+// the body's Euler step follows in place (the force kernel has finished
+// reading the positions).
+template <bool EULER>
 __global__ void reduce_splits_kernel(const float4 *__restrict__ part, int n, int splits,
-                                     float4 *__restrict__ out) {
+                                     float4 *__restrict__ out, EulerFuse eu) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += stride) {
@@ -201,8 +204,16 @@ __global__ void reduce_splits_kernel(const float4 *__restrict__ part, int n, int
             kahan1(hz, cz, v.z);
             kahan1(hw, cw, v.w);
         }
-        out[i] = make_float4(__fsub_rn(hx, cx), __fsub_rn(hy, cy), __fsub_rn(hz, cz),
-                             __fsub_rn(hw, cw));
+        const float4 a = make_float4(__fsub_rn(hx, cx), __fsub_rn(hy, cy), __fsub_rn(hz, cz),
+                                     __fsub_rn(hw, cw));
+        out[i] = a;
+        if (EULER) {
+            float4 x = eu.pos_out[i];
+            float4 v = eu.vel[i];
+            euler_body(x, v, a, eu.dt);
+            eu.pos_out[i] = x;
+            eu.vel[i] = v;
+        }
     }
 }
 
@@ -260,11 +271,15 @@ cudaError_t launch_tiled(int variant, const Problem &pr, int num_ib, int splits,
 }
 
 cudaError_t launch_reduce_splits(const float4 *part, int n, int splits, float4 *out, int sm_count,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, const EulerFuse *euler) {
     const int threads = 256;
     const int64_t want = (static_cast<int64_t>(n) + threads - 1) / threads;
     const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sm_count) * 8));
-    reduce_splits_kernel<<<grid, threads, 0, stream>>>(part, n, splits, out);
+    if (euler != nullptr)
+        reduce_splits_kernel<true><<<grid, threads, 0, stream>>>(part, n, splits, out, *euler);
+    else
+        reduce_splits_kernel<false><<<grid, threads, 0, stream>>>(part, n, splits, out,
+                                                                  EulerFuse{nullptr, nullptr, 0.f});
     return cudaGetLastError();
 }
 

@@ -449,6 +449,37 @@ cudaError_t launch_planned(const nbody_plan &plan, const nbody::Problem &pr, flo
     return e;
 }
 
+// One time step: the planned force evaluation, then the Euler update.  When
+// the plan ends in a reduction kernel, the update runs inside it, body by
+// body, as each final (a, p) is formed (same arithmetic, one launch and one
+// pass over the bodies fewer); otherwise the Euler kernel follows.
+cudaError_t launch_step(const nbody_plan &plan, const nbody::Problem &pr, float4 *acc,
+                        float4 *scratch, int sm_count, float4 *pos, float4 *vel, float dt,
+                        cudaStream_t stream) {
+    const nbody::EulerFuse eu = {pos, vel, dt};
+    if (plan.path == NBODY_PATH_SYMMETRIC && plan.scratch_bytes > 0) {
+        const int block = plan.threads * plan.i_per_thread;
+        float4 *jpart = scratch + static_cast<int64_t>(plan.splits) * pr.nt;
+        cudaError_t e = nbody::launch_sym(plan.variant, pr.targets, pr.nt, pr.eps2,
+                                          plan.num_iblocks, plan.splits, scratch, jpart, stream);
+        if (e == cudaSuccess)
+            e = nbody::launch_reduce_sym(scratch, plan.splits, jpart, pr.nt, block,
+                                         plan.num_iblocks, acc, sm_count, stream, &eu);
+        return e;
+    }
+    if (plan.path == NBODY_PATH_TILED && plan.splits > 1) {
+        const int ntiles = static_cast<int>(ceil_div(pr.ns, plan.tile));
+        cudaError_t e = nbody::launch_tiled(plan.variant, pr, plan.num_iblocks, plan.splits,
+                                            plan.tiles_per_split, ntiles, scratch, stream);
+        if (e == cudaSuccess)
+            e = nbody::launch_reduce_splits(scratch, pr.nt, plan.splits, acc, sm_count, stream, &eu);
+        return e;
+    }
+    cudaError_t e = launch_planned(plan, pr, acc, scratch, sm_count, stream);
+    if (e == cudaSuccess) e = nbody::launch_euler(pos, vel, acc, pr.nt, dt, sm_count, stream);
+    return e;
+}
+
 Occupancy device_occupancy(const DeviceState *dev) {
     return {dev->tiled_occ, dev->cluster_occ, dev->sym_occ};
 }
@@ -486,13 +517,16 @@ nbody_status run_forces(const nbody::Problem &pr, const nbody_forces_opts *opts,
 // One step (forces, then Euler) is captured once into a CUDA graph on an
 // internal stream and replayed `steps` times on the caller's stream, so a
 // step costs one graph launch instead of two or three kernel launches from
-// the host.  On the cluster path (small N) a second graph holds two steps
-// whose Euler update is fused into the force kernel, the positions going
-// from pos_mass to a library-owned second buffer and back; steps run in
-// pairs through it, and an odd last step through the one-step graph.  One graph per device is cached, keyed by every argument but the
-// step count; its split scratch (if any) lives as long as the graph.  When
-// the key changes, the old graph is destroyed (deferred until it finishes)
-// and its scratch freed in stream order behind its last launch.
+// the host.  Where the forces end in a reduction kernel (the symmetric path,
+// or the tiled path with split sources), the Euler update runs inside it.
+// On the cluster path (small N) a second graph holds two steps whose Euler
+// update is fused into the force kernel, the positions going from pos_mass
+// to a library-owned second buffer and back; steps run in pairs through it,
+// and an odd last step through the one-step graph.  One graph per device is
+// cached, keyed by every argument but the step count; its split scratch (if
+// any) lives as long as the graph.  When the key changes, the old graph is
+// destroyed (deferred until it finishes) and its scratch freed in stream
+// order behind its last launch.
 
 struct SimKey {
     const float *pm;
@@ -584,11 +618,8 @@ nbody_status sim_build(int dev_id, DeviceState *dev, const SimKey &k, SimGraph &
     const nbody::Problem pr = {k.pm, k.pm, ni, ni, k.eps2};
     cudaGraphExec_t exec = nullptr, exec2 = nullptr;
     e = capture_graph(cap, [&](cudaStream_t st) {
-        cudaError_t el = launch_planned(plan, pr, acc, static_cast<float4 *>(scratch),
-                                        dev->sm_count, st);
-        if (el == cudaSuccess)
-            el = nbody::launch_euler(pos, vel, acc, ni, k.dt, dev->sm_count, st);
-        return el;
+        return launch_step(plan, pr, acc, static_cast<float4 *>(scratch), dev->sm_count, pos, vel,
+                           k.dt, st);
     }, &exec);
     // Small N: two steps per replay with the Euler update fused into the
     // cluster kernel, positions alternating between pos_mass and pos_b.

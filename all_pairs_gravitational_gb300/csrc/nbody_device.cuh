@@ -78,6 +78,19 @@ __device__ __forceinline__ void kahan1(float &hi, float &lo, float x) {
     hi = t;
 }
 
+// One body's explicit Euler step, positions first: x <- x + dt v with the old
+// v, then v <- v + dt a, every product and sum rounded on its own
+// (__fmul_rn/__fadd_rn cannot be contracted into an FMA); x.w and v.w pass
+// through.  The lecture's integrate() kernel (slides 15 and 40).
+__device__ __forceinline__ void euler_body(float4 &x, float4 &v, const float4 &a, float dt) {
+    x.x = __fadd_rn(x.x, __fmul_rn(dt, v.x));
+    x.y = __fadd_rn(x.y, __fmul_rn(dt, v.y));
+    x.z = __fadd_rn(x.z, __fmul_rn(dt, v.z));
+    v.x = __fadd_rn(v.x, __fmul_rn(dt, a.x));
+    v.y = __fadd_rn(v.y, __fmul_rn(dt, a.y));
+    v.z = __fadd_rn(v.z, __fmul_rn(dt, a.z));
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

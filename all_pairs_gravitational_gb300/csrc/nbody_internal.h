@@ -33,10 +33,11 @@ const TiledVariant &tiled_variant(int v);
 cudaError_t launch_tiled(int variant, const Problem &pr, int num_ib, int splits,
                          int tiles_per_split, int ntiles, float4 *out, cudaStream_t stream);
 
-// Euler update applied by a force kernel as it stores each target's result:
+// Euler update applied by a kernel as it stores each body's result:
 // pos_out = pos + dt * vel (old vel), then vel += dt * a, every product and
-// sum rounded on its own.  pos_out must not be the targets array (other CTAs
-// are still reading it); the mass is copied.
+// sum rounded on its own; the mass is copied.  In a force kernel pos_out must
+// not be the targets array (other CTAs are still reading it); in a reduction
+// kernel, which runs after the force kernel, it is the positions themselves.
 struct EulerFuse {
     float4 *pos_out;
     float4 *vel;
@@ -89,13 +90,18 @@ cudaError_t launch_sym(int variant, const float *bodies, int n, float eps2, int 
                        float4 *ipart, float4 *jpart, cudaStream_t stream);
 
 // out[i] = the splits i-side slots of body i, then its j-side slots, in a
-// fixed order, compensated (block = T bodies).
+// fixed order, compensated (block = T bodies).  With `euler`, each body's
+// Euler step follows in place (euler->pos_out = the positions the force
+// kernel read, which it has finished reading).
 cudaError_t launch_reduce_sym(const float4 *ipart, int splits, const float4 *jpart, int n,
-                              int block, int nb, float4 *out, int sm_count, cudaStream_t stream);
+                              int block, int nb, float4 *out, int sm_count, cudaStream_t stream,
+                              const EulerFuse *euler = nullptr);
 
-// out[i] = sum over s of part[s * n + i], in the order s = 0, 1, ..., compensated.
+// out[i] = sum over s of part[s * n + i], in the order s = 0, 1, ..., compensated;
+// with `euler`, each body's Euler step follows in place, as above.
 cudaError_t launch_reduce_splits(const float4 *part, int n, int splits, float4 *out,
-                                 int sm_count, cudaStream_t stream);
+                                 int sm_count, cudaStream_t stream,
+                                 const EulerFuse *euler = nullptr);
 
 cudaError_t launch_euler(float4 *pos_mass, float4 *vel, const float4 *acc_pot, int n,
                          float dt, int sm_count, cudaStream_t stream);

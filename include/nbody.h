@@ -114,8 +114,10 @@ nbody_status nbody_forces_ts(const float *targets, int64_t nt, const float *sour
 /*
  * nbody_simulate -- `steps` explicit Euler steps of the self-gravitating
  * system, device-resident: each step is nbody_forces(pos_mass -> acc_pot)
- * followed by nbody_euler_step, exactly as the two calls would do it (same
- * kernels, bit-identical results).  It replaces the host loop of the
+ * followed by nbody_euler_step, with the same arithmetic as the two calls and
+ * bit-identical results (where the forces end in a reduction kernel, the
+ * Euler update runs inside it; at small n it runs inside the force kernel).
+ * It replaces the host loop of the
  * lecture's program (slide 13, the commented time loop) and of the Aizu host
  * flow (No.10, upload / run / read back / integrate on the host).
  *
