@@ -177,7 +177,7 @@ __device__ __forceinline__ void reduce_and_store(WarpAcc<K / 2> &acc, float4 (*r
         const int64_t i = static_cast<int64_t>(ib) * BI + slot;
         if (i < pr.nt) {
             const float4 a = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y),
-                                         __fsub_rn(h.z, c.z), -__fsub_rn(h.w, c.w));
+                                         __fsub_rn(h.z, c.z), POT ? -__fsub_rn(h.w, c.w) : 0.f);
             out[i] = a;
             if (EULER) {   // the step of euler.cu, on this body, positions first
                 float4 x = __ldg(reinterpret_cast<const float4 *>(pr.targets) + i);
@@ -305,11 +305,16 @@ cudaError_t launch_tiled_cluster(const Problem &pr, int num_ib, int cluster, int
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    const EulerFuse none = {nullptr, nullptr, 0.f};
     if (eu != nullptr)
-        return cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true, true>, pr, tpc, ntiles,
-                                  out, *eu);
-    return cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true, false>, pr, tpc, ntiles,
-                              out, EulerFuse{nullptr, nullptr, 0.f});
+        return pr.pot ? cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true, true>, pr,
+                                           tpc, ntiles, out, *eu)
+                      : cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, false, true>, pr,
+                                           tpc, ntiles, out, *eu);
+    return pr.pot ? cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true, false>, pr, tpc,
+                                       ntiles, out, none)
+                  : cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, false, false>, pr, tpc,
+                                       ntiles, out, none);
 }
 
 template <int K, int W>
@@ -327,15 +332,25 @@ cudaError_t launch_whole(const Problem &pr, int num_ib, int cluster, int tpc, fl
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    const EulerFuse none = {nullptr, nullptr, 0.f};
     if (eu != nullptr)
-        return cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, true, true>, pr, tpc, out,
-                                  *eu);
-    return cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, true, false>, pr, tpc, out,
-                              EulerFuse{nullptr, nullptr, 0.f});
+        return pr.pot ? cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, true, true>, pr,
+                                           tpc, out, *eu)
+                      : cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, false, true>, pr,
+                                           tpc, out, *eu);
+    return pr.pot ? cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, true, false>, pr, tpc,
+                                       out, none)
+                  : cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, false, false>, pr,
+                                       tpc, out, none);
 }
 
-#define NBODY_CLUSTER(K, W, P) {K, W, P, false, reinterpret_cast<const void *>(&forces_cluster_kernel<K, W, P, true, false>)}
-#define NBODY_CLUSTER_WHOLE(K, W) {K, W, kClusterTile, true, reinterpret_cast<const void *>(&forces_cluster_whole_kernel<K, W, true, false>)}
+#define NBODY_CLUSTER(K, W, P)                                                             \
+    {K, W, P, false, reinterpret_cast<const void *>(&forces_cluster_kernel<K, W, P, true, false>), \
+     reinterpret_cast<const void *>(&forces_cluster_kernel<K, W, P, false, false>)}
+#define NBODY_CLUSTER_WHOLE(K, W)                                                          \
+    {K, W, kClusterTile, true,                                                             \
+     reinterpret_cast<const void *>(&forces_cluster_whole_kernel<K, W, true, false>),      \
+     reinterpret_cast<const void *>(&forces_cluster_whole_kernel<K, W, false, false>)}
 
 const ClusterVariant kVariants[] = {
     NBODY_CLUSTER(2, 4, 128),   // 0: default

@@ -13,11 +13,12 @@
 // Decomposition.  Bodies are cut into nb blocks of T = 32 W K.  Block pair
 // (I, J), I != J, is evaluated once, by row I when J = I + d (mod nb) with
 // 1 <= d <= H = (nb - 1) / 2, and for even nb also d = nb / 2 by the row
-// I < nb / 2 only.  Row I also evaluates its own block against itself, one
-// way only (the i-side), which includes every self pair: it adds 0 to a and
-// -m_i / eps to p, with no branch (lecture slide 12).  A row's work is a list
-// of units -- SUB bodies of one block J -- that may be split into S pieces
-// (one CTA each) so that nb x S CTAs fill the GPU.
+// I < nb / 2 only.  Row I also evaluates its own block against itself (d = 0),
+// one way only (the i-side), which includes every self pair: it adds 0 to a
+// and -m_i / eps to p, with no branch (lecture slide 12).  The distances are
+// taken in groups of D; in each group a row's work is a list of units -- SUB
+// bodies of one block J -- cut into P pieces, one CTA each, so that the
+// launch fills the GPU.  A launch evaluates one or more consecutive groups.
 //
 // Per CTA: W warps, each holding K targets per lane (K/2 packed f32x2 pairs)
 // for the whole piece.  A unit is streamed 32 bodies at a time: lane l loads
@@ -30,9 +31,10 @@
 // Sums and determinism.  The i-side is folded into Kahan totals every 32
 // sources (the acceleration) and every 1024 (the potential), as in the tiled
 // kernel.  After each unit, the warps' j-side sums for its SUB sources are
-// added in warp order and written to slot d - 1 of a partial array; the i-side
-// totals of piece s go to slot s of another.  A second kernel adds, for every
-// body, its S i-side slots and its H (or H + 1) j-side slots in a fixed
+// added in warp order and written to the group's j-side slot of distance d;
+// the i-side totals of piece k go to the group's i-side slot k.  The
+// reduction kernel (reduce.cu) adds, for every body, each group's i-side
+// slots and then the j-side slots that reach it, group by group, in a fixed
 // order, Kahan-compensated.  No atomics: results are bit-reproducible.
 //
 // Bodies past n are loaded as zeros: a zero mass adds exactly 0 to the other
@@ -67,8 +69,8 @@ __device__ __forceinline__ float4 body_or_zero(const float4 *__restrict__ bodies
 
 // One chunk both ways: the lane's targets against the 32 home sources of the
 // warp, i-side into (ax, ay, az, pp), j-side returned for this lane's home
-// source as (ax, ay, az, -p).
-template <int KP, int U, bool GF>
+// source as (ax, ay, az, -p) (-p = 0 without the potential).
+template <int KP, int U, bool GF, bool POT>
 __device__ __forceinline__ float4 chunk_sym(float4 home, const f2 (&xi)[KP], const f2 (&yi)[KP],
                                             const f2 (&zi)[KP], const f2 (&nmi)[KP], f2 e2,
                                             f2 (&ax)[KP], f2 (&ay)[KP], f2 (&az)[KP],
@@ -96,12 +98,12 @@ __device__ __forceinline__ float4 chunk_sym(float4 home, const f2 (&xi)[KP], con
             ax[q] = f2_fma(sc, g.dx, ax[q]);
             ay[q] = f2_fma(sc, g.dy, ay[q]);
             az[q] = f2_fma(sc, g.dz, az[q]);
-            pp[q] = f2_fma(sj.m, g.inv, pp[q]);           // + m_j / d
+            if (POT) pp[q] = f2_fma(sj.m, g.inv, pp[q]);  // + m_j / d
             const f2 nsc = f2_mul(nmi[q], inv3);          // -m_i / d^3
             tx = f2_fma(nsc, g.dx, tx);
             ty = f2_fma(nsc, g.dy, ty);
             tz = f2_fma(nsc, g.dz, tz);
-            tp = f2_fma(nmi[q], g.inv, tp);               // - m_i / d
+            if (POT) tp = f2_fma(nmi[q], g.inv, tp);      // - m_i / d
         }
         float a, b;
         f2_unpack(tx, a, b);
@@ -110,15 +112,17 @@ __device__ __forceinline__ float4 chunk_sym(float4 home, const f2 (&xi)[KP], con
         jy += __shfl_xor_sync(0xffffffffu, a + b, s);
         f2_unpack(tz, a, b);
         jz += __shfl_xor_sync(0xffffffffu, a + b, s);
-        f2_unpack(tp, a, b);
-        jp += __shfl_xor_sync(0xffffffffu, a + b, s);
+        if (POT) {
+            f2_unpack(tp, a, b);
+            jp += __shfl_xor_sync(0xffffffffu, a + b, s);
+        }
     }
     return make_float4(jx, jy, jz, jp);
 }
 
 // One chunk of the row's own block: i-side only (the pair law of the tiled
 // kernel), self pairs included.
-template <int KP, int U>
+template <int KP, int U, bool POT>
 __device__ __forceinline__ void chunk_diag(float4 home, const f2 (&xi)[KP], const f2 (&yi)[KP],
                                            const f2 (&zi)[KP], f2 e2, f2 (&ax)[KP], f2 (&ay)[KP],
                                            f2 (&az)[KP], f2 (&pp)[KP]) {
@@ -132,15 +136,16 @@ __device__ __forceinline__ void chunk_diag(float4 home, const f2 (&xi)[KP], cons
 #pragma unroll
         for (int q = 0; q < KP; ++q) {
             const Geom g = pair_geom(sj, xi[q], yi[q], zi[q], e2);
-            pp[q] = f2_add(pp[q], pair_accumulate(g, sj.m, ax[q], ay[q], az[q]));
+            const f2 tm = pair_accumulate(g, sj.m, ax[q], ay[q], az[q]);
+            if (POT) pp[q] = f2_add(pp[q], tm);
         }
     }
 }
 
-template <int K, int W, int SUB, int MINB, int U, bool GF>
+template <int K, int W, int SUB, int MINB, int U, bool GF, bool POT>
 __global__ void __launch_bounds__(W * 32, MINB)
-forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, int splits,
-                  float4 *__restrict__ ipart, float4 *__restrict__ jpart) {
+forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, int P, int D,
+                  int g0, float4 *__restrict__ parts, int64_t gstride) {
     using S = SymShape<K, W, SUB>;
     constexpr int KP = S::KP, NT = S::NT, T = S::T, SPB = S::SPB, CPU = S::CPU;
     constexpr int FOLD_P = 32;   // chunks between folds of the potential (1024 sources)
@@ -151,13 +156,21 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
     const int tid = static_cast<int>(threadIdx.x);
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int row = static_cast<int>(blockIdx.x % static_cast<unsigned>(nb));
-    const int piece = static_cast<int>(blockIdx.x / static_cast<unsigned>(nb));
+    const unsigned b = blockIdx.x;
+    const int row = static_cast<int>(b % static_cast<unsigned>(nb));
+    const unsigned rest = b / static_cast<unsigned>(nb);
+    const int piece = static_cast<int>(rest % static_cast<unsigned>(P));
+    const int gl = static_cast<int>(rest / static_cast<unsigned>(P));
+    // this group's distances for this row: [dlo, dhi)
+    const int dlo = (g0 + gl) * D;
     const int H = (nb - 1) / 2;
-    const bool extra = (nb % 2 == 0) && row < nb / 2;
-    const int64_t units = static_cast<int64_t>(1 + H + (extra ? 1 : 0)) * SPB;
-    const int64_t u0 = units * piece / splits;
-    const int64_t u1 = units * (piece + 1) / splits;
+    const int dmax = H + ((nb % 2 == 0 && row < nb / 2) ? 1 : 0);
+    const int dhi = min(dlo + D, dmax + 1);
+    const int64_t units = dhi > dlo ? static_cast<int64_t>(dhi - dlo) * SPB : 0;
+    const int64_t u0 = units * piece / P;
+    const int64_t u1 = units * (piece + 1) / P;
+    const int jbase = max(dlo, 1);          // distance of the group's first j-side slot
+    float4 *gparts = parts + static_cast<int64_t>(gl) * gstride;
 
     Totals<KP, NT, true> tot;
     tot.s = reinterpret_cast<f2 (*)[NT]>(smem + S::jacc_bytes);
@@ -186,7 +199,7 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
     auto home_index = [&](int64_t k) -> int64_t {
         const int64_t u = u0 + k / CPU;
         const int c = static_cast<int>(k % CPU);
-        const int d = static_cast<int>(u / SPB);
+        const int d = dlo + static_cast<int>(u / SPB);
         const int sub = static_cast<int>(u % SPB);
         int J = row + d;
         if (J >= nb) J -= nb;
@@ -198,7 +211,7 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
     int64_t k = 0;
     int since_p = 0;
     for (int64_t u = u0; u < u1; ++u) {
-        const int d = static_cast<int>(u / SPB);
+        const int d = dlo + static_cast<int>(u / SPB);
         const int buf = static_cast<int>(u & 1);
 #pragma unroll 1
         for (int c = 0; c < CPU; ++c, ++k) {
@@ -206,9 +219,9 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
             if (k + 1 < nchunks) next = body_or_zero(bodies, home_index(k + 1), n);
             if (d != 0) {
                 jacc[buf][warp][c * 32 + lane] =
-                    chunk_sym<KP, U, GF>(home, xi, yi, zi, nmi, e2, ax, ay, az, pp);
+                    chunk_sym<KP, U, GF, POT>(home, xi, yi, zi, nmi, e2, ax, ay, az, pp);
             } else {
-                chunk_diag<KP, U>(home, xi, yi, zi, e2, ax, ay, az, pp);
+                chunk_diag<KP, U, POT>(home, xi, yi, zi, e2, ax, ay, az, pp);
             }
 #pragma unroll
             for (int q = 0; q < KP; ++q) {
@@ -216,7 +229,7 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
                 tot.fold(q, 1, ay[q]);
                 tot.fold(q, 2, az[q]);
             }
-            if (++since_p == FOLD_P) {
+            if (POT && ++since_p == FOLD_P) {
                 since_p = 0;
 #pragma unroll
                 for (int q = 0; q < KP; ++q) tot.fold(q, 3, pp[q]);
@@ -235,75 +248,34 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
                 kahan1(hx, cx, v.x);
                 kahan1(hy, cy, v.y);
                 kahan1(hz, cz, v.z);
-                kahan1(hw, cw, v.w);
+                if (POT) kahan1(hw, cw, v.w);
             }
             int J = row + d;
             if (J >= nb) J -= nb;
             const int64_t j = static_cast<int64_t>(J) * T + static_cast<int>(u % SPB) * SUB + tid;
             if (j < n)
-                jpart[static_cast<int64_t>(d - 1) * n + j] =
+                gparts[static_cast<int64_t>(P + d - jbase) * n + j] =
                     make_float4(__fsub_rn(hx, cx), __fsub_rn(hy, cy), __fsub_rn(hz, cz),
                                 __fsub_rn(hw, cw));
         }
     }
+    if (POT) {
 #pragma unroll
-    for (int q = 0; q < KP; ++q) tot.fold(q, 3, pp[q]);
+        for (int q = 0; q < KP; ++q) tot.fold(q, 3, pp[q]);
+    }
 
-    float4 *dst = ipart + static_cast<int64_t>(piece) * n;
+    float4 *dst = gparts + static_cast<int64_t>(piece) * n;
 #pragma unroll
     for (int q = 0; q < KP; ++q) {
-        float x0, x1, y0, y1, z0, z1, p0, p1;
+        float x0, x1, y0, y1, z0, z1, p0 = 0.f, p1 = 0.f;
         f2_unpack(tot.value(q, 0), x0, x1);
         f2_unpack(tot.value(q, 1), y0, y1);
         f2_unpack(tot.value(q, 2), z0, z1);
-        f2_unpack(tot.value(q, 3), p0, p1);
+        if (POT) f2_unpack(tot.value(q, 3), p0, p1);
         const int64_t i0 = ibase + 64 * q;
         const int64_t i1 = i0 + 32;
-        if (i0 < n) dst[i0] = make_float4(x0, y0, z0, -p0);
-        if (i1 < n) dst[i1] = make_float4(x1, y1, z1, -p1);
-    }
-}
-
-// out[i] = the S i-side slots of body i, then its j-side slots (H of them,
-// H + 1 for a body of block >= nb / 2 when nb is even), added in that fixed
-// order with compensation.  With EULER, the body's Euler step follows in
-// place (the force kernel has finished reading the positions).
-template <bool EULER>
-__global__ void reduce_sym_kernel(const float4 *__restrict__ ipart, int splits,
-                                  const float4 *__restrict__ jpart, int n, int block, int nb,
-                                  float4 *__restrict__ out, EulerFuse eu) {
-    const int H = (nb - 1) / 2;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-         i += stride) {
-        float hx = 0.f, hy = 0.f, hz = 0.f, hw = 0.f;
-        float cx = 0.f, cy = 0.f, cz = 0.f, cw = 0.f;
-        for (int s = 0; s < splits; ++s) {
-            const float4 v = __ldg(ipart + static_cast<int64_t>(s) * n + i);
-            kahan1(hx, cx, v.x);
-            kahan1(hy, cy, v.y);
-            kahan1(hz, cz, v.z);
-            kahan1(hw, cw, v.w);
-        }
-        const int blk = static_cast<int>(i / block);
-        const int slots = H + ((nb % 2 == 0 && blk >= nb / 2) ? 1 : 0);
-        for (int s = 0; s < slots; ++s) {
-            const float4 v = __ldg(jpart + static_cast<int64_t>(s) * n + i);
-            kahan1(hx, cx, v.x);
-            kahan1(hy, cy, v.y);
-            kahan1(hz, cz, v.z);
-            kahan1(hw, cw, v.w);
-        }
-        const float4 a = make_float4(__fsub_rn(hx, cx), __fsub_rn(hy, cy), __fsub_rn(hz, cz),
-                                     __fsub_rn(hw, cw));
-        out[i] = a;
-        if (EULER) {
-            float4 x = eu.pos_out[i];
-            float4 v = eu.vel[i];
-            euler_body(x, v, a, eu.dt);
-            eu.pos_out[i] = x;
-            eu.vel[i] = v;
-        }
+        if (i0 < n) dst[i0] = make_float4(x0, y0, z0, POT ? -p0 : 0.f);
+        if (i1 < n) dst[i1] = make_float4(x1, y1, z1, POT ? -p1 : 0.f);
     }
 }
 
@@ -311,16 +283,18 @@ __global__ void reduce_sym_kernel(const float4 *__restrict__ ipart, int splits,
 // unit, the minimum resident CTAs per SM asked of the register allocator, the
 // unroll factor of the 32-step chunk loop, and GF: the geometry and rsqrt of
 // all K/2 target pairs computed before any of their accumulations (the
-// rsqrt latencies overlap).  Variants 0-2 differ only in the block size (W =
-// 8, 4, 2 warps: 2048, 1024, 512 bodies); the planner takes the smaller
-// blocks for smaller n, whose waves they fill better, and variant 0 from
-// about 160K bodies, where fewer partial slots win (3.31e12 interactions/s at
-// 2^20; 118 registers).  Variants 3-5 stay selectable for tests and sweeps.
+// rsqrt latencies overlap).  Each shape is built with and without the
+// potential.  The variants differ only in the block size (W = 8, 4, 2 warps:
+// 2048, 1024, 512 bodies); the planner takes the smaller blocks for smaller
+// n, whose waves they fill better, and variant 0 from about 160K bodies,
+// where fewer partial slots win (3.31e12 interactions/s at 2^20; 118
+// registers).
 // Measured and dropped, each relative to the best shape of its time:
 //   128-body units (1.5-2.5 % slower), 32-body units (2-3 % slower);
 //   K = 6 or 4 (6-12 % slower); K = 2 or 4 with 32-body units and 256- or
 //   512-body blocks (slower than variant 2 at every size from 2048 bodies);
 //   the chunk loop unrolled by 2 or 4 (2-4 % slower);
+//   each target pair's geometry and accumulation in turn (2.4 % slower);
 //   two partners per step side by side (1-9 % slower);
 //   1/d^2 from a MUFU reciprocal instead of a packed multiply, one FMA-pipe
 //   operation fewer per pair (2.5 % slower);
@@ -335,28 +309,32 @@ __global__ void reduce_sym_kernel(const float4 *__restrict__ ipart, int splits,
 #define NBODY_SYM_LIST(X)                     \
     X(8, 8, 64, 2, 1, true)   /* 0: default */ \
     X(8, 4, 64, 4, 1, true)   /* 1 */          \
-    X(8, 2, 64, 8, 1, true)   /* 2 */          \
-    X(8, 8, 64, 2, 2, false)  /* 3 */          \
-    X(6, 8, 64, 2, 1, true)   /* 4 */          \
-    X(4, 8, 64, 2, 1, true)   /* 5 */
+    X(8, 2, 64, 8, 1, true)   /* 2 */
 
-#define NBODY_SYM_ENTRY(K, W, SUB, MINB, U, GF)                                  \
-    {K, W, SUB, MINB, SymShape<K, W, SUB>::smem_bytes,                             \
-     reinterpret_cast<const void *>(&forces_sym_kernel<K, W, SUB, MINB, U, GF>)},
+#define NBODY_SYM_ENTRY(K, W, SUB, MINB, U, GF)                                      \
+    {K, W, SUB, MINB, SymShape<K, W, SUB>::smem_bytes,                                 \
+     reinterpret_cast<const void *>(&forces_sym_kernel<K, W, SUB, MINB, U, GF, true>), \
+     reinterpret_cast<const void *>(&forces_sym_kernel<K, W, SUB, MINB, U, GF, false>)},
 
 const SymVariant kSymVariants[] = {NBODY_SYM_LIST(NBODY_SYM_ENTRY)};
 
 template <int K, int W, int SUB, int MINB, int U, bool GF>
-cudaError_t launch_sym_variant(const float *bodies, int n, float eps2, int nb, int splits,
-                               float4 *ipart, float4 *jpart, cudaStream_t stream) {
-    const unsigned grid = static_cast<unsigned>(nb) * static_cast<unsigned>(splits);
-    forces_sym_kernel<K, W, SUB, MINB, U, GF>
-        <<<grid, W * 32, SymShape<K, W, SUB>::smem_bytes, stream>>>(
-            reinterpret_cast<const float4 *>(bodies), n, eps2, nb, splits, ipart, jpart);
+cudaError_t launch_sym_variant(const float *bodies, int n, float eps2, bool pot,
+                               const SymLaunch &sl, float4 *parts, cudaStream_t stream) {
+    const unsigned grid = static_cast<unsigned>(sl.nb) * static_cast<unsigned>(sl.P) *
+                          static_cast<unsigned>(sl.groups);
+    const float4 *b4 = reinterpret_cast<const float4 *>(bodies);
+    constexpr size_t smem = SymShape<K, W, SUB>::smem_bytes;
+    if (pot)
+        forces_sym_kernel<K, W, SUB, MINB, U, GF, true><<<grid, W * 32, smem, stream>>>(
+            b4, n, eps2, sl.nb, sl.P, sl.D, sl.g0, parts, sl.gstride);
+    else
+        forces_sym_kernel<K, W, SUB, MINB, U, GF, false><<<grid, W * 32, smem, stream>>>(
+            b4, n, eps2, sl.nb, sl.P, sl.D, sl.g0, parts, sl.gstride);
     return cudaGetLastError();
 }
 
-typedef cudaError_t (*SymLauncher)(const float *, int, float, int, int, float4 *, float4 *,
+typedef cudaError_t (*SymLauncher)(const float *, int, float, bool, const SymLaunch &, float4 *,
                                    cudaStream_t);
 
 #define NBODY_SYM_LAUNCHER(K, W, SUB, MINB, U, GF) &launch_sym_variant<K, W, SUB, MINB, U, GF>,
@@ -372,25 +350,23 @@ int sym_variant_count() { return static_cast<int>(sizeof(kSymVariants) / sizeof(
 
 const SymVariant &sym_variant(int v) { return kSymVariants[v]; }
 
-cudaError_t launch_sym(int variant, const float *bodies, int n, float eps2, int nb, int splits,
-                       float4 *ipart, float4 *jpart, cudaStream_t stream) {
-    if (variant < 0 || variant >= sym_variant_count()) return cudaErrorInvalidValue;
-    return kSymLaunchers[variant](bodies, n, eps2, nb, splits, ipart, jpart, stream);
+int sym_group_jslots(int nb, int D) {
+    const int nd = sym_ndist(nb);
+    const int groups = (nd + D - 1) / D;
+    int best = 0;
+    for (int g = 0; g < groups && g < 2; ++g) {   // group 0 lacks d = 0's slot; group 1 is full
+        const int lo = std::max(g * D, 1);
+        const int hi = std::min((g + 1) * D, nd);
+        best = std::max(best, hi - lo);
+    }
+    return best;
 }
 
-cudaError_t launch_reduce_sym(const float4 *ipart, int splits, const float4 *jpart, int n,
-                              int block, int nb, float4 *out, int sm_count, cudaStream_t stream,
-                              const EulerFuse *euler) {
-    const int threads = 256;
-    const int64_t want = (static_cast<int64_t>(n) + threads - 1) / threads;
-    const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sm_count) * 8));
-    if (euler != nullptr)
-        reduce_sym_kernel<true><<<grid, threads, 0, stream>>>(ipart, splits, jpart, n, block, nb,
-                                                              out, *euler);
-    else
-        reduce_sym_kernel<false><<<grid, threads, 0, stream>>>(ipart, splits, jpart, n, block, nb,
-                                                               out, EulerFuse{nullptr, nullptr, 0.f});
-    return cudaGetLastError();
+cudaError_t launch_sym(int variant, const float *bodies, int n, float eps2, bool pot,
+                       const SymLaunch &sl, float4 *parts, cudaStream_t stream) {
+    if (variant < 0 || variant >= sym_variant_count()) return cudaErrorInvalidValue;
+    if (sl.nb < 1 || sl.P < 1 || sl.D < 1 || sl.groups < 1) return cudaErrorInvalidValue;
+    return kSymLaunchers[variant](bodies, n, eps2, pot, sl, parts, stream);
 }
 
 }  // namespace nbody

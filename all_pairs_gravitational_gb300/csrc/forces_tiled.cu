@@ -5,7 +5,8 @@
 // may be split into S pieces so that (i-blocks x pieces) fills the GPU's CTA
 // slots evenly (with one piece per i-block, N = 2^20 would leave part of the
 // last wave idle on 152 SMs).  S > 1 writes fp32 partials, which a second
-// kernel adds in a fixed order.
+// kernel (reduce.cu) adds in a fixed order; a launch may cover a subset of
+// the pieces when the workspace holds fewer than S partial arrays.
 //
 // Per CTA:
 //   * each thread keeps K targets in registers, as K/2 packed f32x2 pairs
@@ -54,7 +55,7 @@ constexpr int kFoldJ = 32;
 //      instead of 13), for bodies whose sum cancels heavily.
 template <int K, int NT, int P, int MINB, bool TSMEM, int U, int MODE, bool POT>
 __global__ void __launch_bounds__(NT, MINB)
-forces_tiled_kernel(const Problem pr, int num_ib, int tiles_per_split, int ntiles,
+forces_tiled_kernel(const Problem pr, int num_ib, int piece0, int tiles_per_split, int ntiles,
                     float4 *__restrict__ out) {
     static_assert(K % 2 == 0, "targets are processed in f32x2 pairs");
     static_assert(MODE == 0 || MODE == 2 || MODE == 3, "unknown loop mode");
@@ -68,7 +69,7 @@ forces_tiled_kernel(const Problem pr, int num_ib, int tiles_per_split, int ntile
     const int tid = static_cast<int>(threadIdx.x);
     const int ib = static_cast<int>(blockIdx.x % static_cast<unsigned>(num_ib));
     const int split = static_cast<int>(blockIdx.x / static_cast<unsigned>(num_ib));
-    const int t_begin = split * tiles_per_split;
+    const int t_begin = (piece0 + split) * tiles_per_split;
     const int t_end = min(t_begin + tiles_per_split, ntiles);
     const int64_t ibase = static_cast<int64_t>(ib) * (NT * K) + tid;
 
@@ -181,39 +182,8 @@ forces_tiled_kernel(const Problem pr, int num_ib, int tiles_per_split, int ntile
         if (POT) f2_unpack(tot.value(q, 3), p0, p1);
         const int64_t i0 = ibase + (2 * q) * NT;
         const int64_t i1 = ibase + (2 * q + 1) * NT;
-        if (i0 < pr.nt) dst[i0] = make_float4(x0, y0, z0, -p0);
-        if (i1 < pr.nt) dst[i1] = make_float4(x1, y1, z1, -p1);
-    }
-}
-
-// Fixed-order compensated sum of the S partials of each body; with EULER,
-// the body's Euler step follows in place (the force kernel has finished
-// reading the positions).
-template <bool EULER>
-__global__ void reduce_splits_kernel(const float4 *__restrict__ part, int n, int splits,
-                                     float4 *__restrict__ out, EulerFuse eu) {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-         i += stride) {
-        float hx = 0.f, hy = 0.f, hz = 0.f, hw = 0.f;
-        float cx = 0.f, cy = 0.f, cz = 0.f, cw = 0.f;
-        for (int s = 0; s < splits; ++s) {
-            const float4 v = __ldg(part + static_cast<int64_t>(s) * n + i);
-            kahan1(hx, cx, v.x);
-            kahan1(hy, cy, v.y);
-            kahan1(hz, cz, v.z);
-            kahan1(hw, cw, v.w);
-        }
-        const float4 a = make_float4(__fsub_rn(hx, cx), __fsub_rn(hy, cy), __fsub_rn(hz, cz),
-                                     __fsub_rn(hw, cw));
-        out[i] = a;
-        if (EULER) {
-            float4 x = eu.pos_out[i];
-            float4 v = eu.vel[i];
-            euler_body(x, v, a, eu.dt);
-            eu.pos_out[i] = x;
-            eu.vel[i] = v;
-        }
+        if (i0 < pr.nt) dst[i0] = make_float4(x0, y0, z0, POT ? -p0 : 0.f);
+        if (i1 < pr.nt) dst[i1] = make_float4(x1, y1, z1, POT ? -p1 : 0.f);
     }
 }
 
@@ -235,21 +205,28 @@ __global__ void reduce_splits_kernel(const float4 *__restrict__ part, int n, int
     X(2, 256, 128, 4, false, 4, 2)  /* 6 */                  \
     X(4, 256, 128, 2, false, 4, 3)  /* 7: compensated */
 
-#define NBODY_TILED_ENTRY(K, NT, P, MINB, TS, U, MODE) \
-    {K, NT, P, reinterpret_cast<const void *>(&forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, true>)},
+#define NBODY_TILED_ENTRY(K, NT, P, MINB, TS, U, MODE)                                  \
+    {K, NT, P,                                                                         \
+     reinterpret_cast<const void *>(&forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, true>), \
+     reinterpret_cast<const void *>(&forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, false>)},
 
 const TiledVariant kVariants[] = {NBODY_TILED_LIST(NBODY_TILED_ENTRY)};
 
 template <int K, int NT, int P, int MINB, bool TS, int U, int MODE>
-cudaError_t launch_variant(const Problem &pr, int num_ib, int splits, int tps, int ntiles,
-                           float4 *out, cudaStream_t stream) {
-    const unsigned grid = static_cast<unsigned>(num_ib) * static_cast<unsigned>(splits);
-    forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, true><<<grid, NT, 0, stream>>>(
-        pr, num_ib, tps, ntiles, out);
+cudaError_t launch_variant(const Problem &pr, int num_ib, int piece0, int pieces, int tps,
+                           int ntiles, float4 *out, cudaStream_t stream) {
+    const unsigned grid = static_cast<unsigned>(num_ib) * static_cast<unsigned>(pieces);
+    if (pr.pot)
+        forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, true><<<grid, NT, 0, stream>>>(
+            pr, num_ib, piece0, tps, ntiles, out);
+    else
+        forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, false><<<grid, NT, 0, stream>>>(
+            pr, num_ib, piece0, tps, ntiles, out);
     return cudaGetLastError();
 }
 
-typedef cudaError_t (*TiledLauncher)(const Problem &, int, int, int, int, float4 *, cudaStream_t);
+typedef cudaError_t (*TiledLauncher)(const Problem &, int, int, int, int, int, float4 *,
+                                     cudaStream_t);
 
 #define NBODY_TILED_LAUNCHER(K, NT, P, MINB, TS, U, MODE) &launch_variant<K, NT, P, MINB, TS, U, MODE>,
 
@@ -264,23 +241,11 @@ int tiled_variant_count() { return static_cast<int>(sizeof(kVariants) / sizeof(k
 
 const TiledVariant &tiled_variant(int v) { return kVariants[v]; }
 
-cudaError_t launch_tiled(int variant, const Problem &pr, int num_ib, int splits, int tps,
-                         int ntiles, float4 *out, cudaStream_t stream) {
+cudaError_t launch_tiled(int variant, const Problem &pr, int num_ib, int piece0, int pieces,
+                         int tps, int ntiles, float4 *out, cudaStream_t stream) {
     if (variant < 0 || variant >= tiled_variant_count()) return cudaErrorInvalidValue;
-    return kLaunchers[variant](pr, num_ib, splits, tps, ntiles, out, stream);
-}
-
-cudaError_t launch_reduce_splits(const float4 *part, int n, int splits, float4 *out, int sm_count,
-                                 cudaStream_t stream, const EulerFuse *euler) {
-    const int threads = 256;
-    const int64_t want = (static_cast<int64_t>(n) + threads - 1) / threads;
-    const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sm_count) * 8));
-    if (euler != nullptr)
-        reduce_splits_kernel<true><<<grid, threads, 0, stream>>>(part, n, splits, out, *euler);
-    else
-        reduce_splits_kernel<false><<<grid, threads, 0, stream>>>(part, n, splits, out,
-                                                                  EulerFuse{nullptr, nullptr, 0.f});
-    return cudaGetLastError();
+    if (num_ib < 1 || pieces < 1 || piece0 < 0) return cudaErrorInvalidValue;
+    return kLaunchers[variant](pr, num_ib, piece0, pieces, tps, ntiles, out, stream);
 }
 
 }  // namespace nbody

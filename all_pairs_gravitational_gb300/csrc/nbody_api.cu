@@ -1,5 +1,6 @@
 // nbody_api.cu -- the C ABI: argument checks, the launch planner, per-device
-// state and dispatch.  See include/nbody.h for the contract of each call.
+// state, workspace handling and dispatch.  See include/nbody.h for the
+// contract of each call.
 #include <cfloat>
 #include <climits>
 #include <cmath>
@@ -24,13 +25,6 @@ nbody_status cuda_fail(cudaError_t e) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool overlap(const void *a, const void *b, int64_t bytes) {
-    const uintptr_t x = reinterpret_cast<uintptr_t>(a);
-    const uintptr_t y = reinterpret_cast<uintptr_t>(b);
-    const uintptr_t len = static_cast<uintptr_t>(bytes);
-    return x < y + len && y < x + len;
-}
-
 // [a, a + a_bytes) and [b, b + b_bytes) share a byte.
 bool overlap2(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a);
@@ -38,17 +32,34 @@ bool overlap2(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes) {
     return x < y + static_cast<uintptr_t>(b_bytes) && y < x + static_cast<uintptr_t>(a_bytes);
 }
 
+bool overlap(const void *a, const void *b, int64_t bytes) { return overlap2(a, bytes, b, bytes); }
+
 nbody_status check_n(int64_t n) {
     return (n < 0 || n > INT32_MAX) ? NBODY_ERR_INVALID_ARG : NBODY_OK;
 }
+
+bool eps2_ok(float eps2) { return std::isfinite(eps2) && eps2 >= FLT_MIN; }
 
 nbody_status check_forces(const float *pm, int64_t n, float eps2, const float *acc) {
     if (check_n(n) != NBODY_OK) return NBODY_ERR_INVALID_ARG;
     if (n == 0) return NBODY_OK;
     if (pm == nullptr || acc == nullptr) return NBODY_ERR_INVALID_ARG;
-    if (!std::isfinite(eps2) || !(eps2 >= FLT_MIN)) return NBODY_ERR_INVALID_ARG;
+    if (!eps2_ok(eps2)) return NBODY_ERR_INVALID_ARG;
     if (!aligned16(pm) || !aligned16(acc)) return NBODY_ERR_MISALIGNED;
     if (overlap(pm, acc, 16 * n)) return NBODY_ERR_ALIAS;
+    return NBODY_OK;
+}
+
+// A caller's workspace: 16-byte aligned, overlapping none of the arrays.
+nbody_status check_workspace(const void *ws, size_t bytes,
+                             std::initializer_list<std::pair<const void *, int64_t>> arrays) {
+    if (bytes == 0 || ws == nullptr) return NBODY_OK;
+    if (bytes > static_cast<size_t>(INT64_MAX)) return NBODY_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return NBODY_ERR_MISALIGNED;
+    for (const auto &a : arrays)
+        if (a.first != nullptr && a.second > 0 &&
+            overlap2(ws, static_cast<int64_t>(bytes), a.first, a.second))
+            return NBODY_ERR_ALIAS;
     return NBODY_OK;
 }
 
@@ -57,26 +68,56 @@ nbody_status check_forces(const float *pm, int64_t n, float eps2, const float *a
 constexpr int kMaxDevices = 64;
 constexpr int kMaxVariants = 32;
 
+struct Occupancy {
+    const int *tiled;
+    const int *cluster;
+    const int *sym;
+};
+
+struct PlanKey {
+    int64_t nt, ns, budget;
+    int32_t all_pairs, sm;
+    nbody_forces_opts opts;
+    bool operator==(const PlanKey &o) const {
+        return nt == o.nt && ns == o.ns && budget == o.budget && all_pairs == o.all_pairs &&
+               sm == o.sm && std::memcmp(&opts, &o.opts, sizeof(opts)) == 0;
+    }
+};
+
+constexpr int kPlanCache = 16;
+
 struct DeviceState {
     bool ready = false;
     int sm_count = 0;
     int tiled_occ[kMaxVariants] = {0};
     int cluster_occ[kMaxVariants] = {0};
     int sym_occ[kMaxVariants] = {0};
-    cudaMemPool_t pool = nullptr;     // stream-ordered scratch for split partials
+    cudaMemPool_t pool = nullptr;     // stream-ordered workspace of the pool-based calls
+    // recently made plans (planning a large n searches thousands of shapes)
+    PlanKey plan_key[kPlanCache];
+    nbody_plan plan_val[kPlanCache];
+    int plan_count = 0;
+    int plan_next = 0;
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
+nbody_status current_device(int *dev) {
+    const cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (*dev < 0 || *dev >= kMaxDevices) return NBODY_ERR_DEVICE;
+    return NBODY_OK;
+}
+
 nbody_status device_state(DeviceState **out) {
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (dev < 0 || dev >= kMaxDevices) return NBODY_ERR_DEVICE;
+    nbody_status st = current_device(&dev);
+    if (st != NBODY_OK) return st;
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState &d = g_dev[dev];
     if (!d.ready) {
+        cudaError_t e;
         int major = 0, minor = 0;
         if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
@@ -91,10 +132,12 @@ nbody_status device_state(DeviceState **out) {
         }
         for (int v = 0; v < nbody::cluster_variant_count() && v < kMaxVariants; ++v) {
             const nbody::ClusterVariant &cv = nbody::cluster_variant(v);
-            if (cv.whole &&
-                (e = cudaFuncSetAttribute(cv.fn_pot, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(nbody::kWholeSmemMax))) != cudaSuccess)
-                return cuda_fail(e);
+            if (cv.whole) {
+                for (const void *fn : {cv.fn_pot, cv.fn_acc})
+                    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(nbody::kWholeSmemMax))) != cudaSuccess)
+                        return cuda_fail(e);
+            }
             // register-limited residency (whole-range launches are further
             // limited by their shared memory, see plan_cluster_variant)
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.cluster_occ[v], cv.fn_pot,
@@ -103,34 +146,63 @@ nbody_status device_state(DeviceState **out) {
         }
         for (int v = 0; v < nbody::sym_variant_count() && v < kMaxVariants; ++v) {
             const nbody::SymVariant &sv = nbody::sym_variant(v);
-            if ((e = cudaFuncSetAttribute(sv.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(sv.smem))) != cudaSuccess)
-                return cuda_fail(e);
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sym_occ[v], sv.fn, sv.warps * 32,
-                                                              sv.smem);
+            for (const void *fn : {sv.fn_pot, sv.fn_acc})
+                if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(sv.smem))) != cudaSuccess)
+                    return cuda_fail(e);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.sym_occ[v], sv.fn_pot,
+                                                              sv.warps * 32, sv.smem);
             if (e != cudaSuccess) return cuda_fail(e);
         }
-        cudaMemPoolProps props = {};
-        props.allocType = cudaMemAllocationTypePinned;
-        props.location.type = cudaMemLocationTypeDevice;
-        props.location.id = dev;
-        if ((e = cudaMemPoolCreate(&d.pool, &props)) != cudaSuccess) return cuda_fail(e);
-        uint64_t keep = UINT64_MAX;   // keep freed blocks for the next call
-        if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
-            return cuda_fail(e);
         d.ready = true;
     }
     *out = &d;
     return NBODY_OK;
 }
 
+// The device's workspace pool, created on first use.  Freed blocks above
+// NBODY_POOL_KEEP_BYTES go back to the system at each synchronisation.
+nbody_status device_pool(DeviceState *d, cudaMemPool_t *pool) {
+    int dev = 0;
+    nbody_status st = current_device(&dev);
+    if (st != NBODY_OK) return st;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (d->pool == nullptr) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        cudaError_t e = cudaMemPoolCreate(&p, &props);
+        if (e != cudaSuccess) return cuda_fail(e);
+        uint64_t keep = static_cast<uint64_t>(NBODY_POOL_KEEP_BYTES);
+        if ((e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+            cudaMemPoolDestroy(p);
+            return cuda_fail(e);
+        }
+        d->pool = p;
+    }
+    *pool = d->pool;
+    return NBODY_OK;
+}
+
 // ---------------------------------------------------------------- planner
+//
+// A plan has two layers.  The decomposition -- the path, the kernel shape,
+// the pieces of each source range and (symmetric path) the groups of
+// distances -- depends only on n, the device and the options, and fixes
+// every partial sum and the order they are added in.  The execution -- how
+// many groups each force launch takes -- follows from the workspace: one
+// pass when all partials fit, otherwise passes of as many groups as fit,
+// with the running compensated total carried between passes exactly.  A
+// workspace too small for one group of the decomposition falls back to a
+// decomposition without partials.
 
 constexpr int kDefaultTiledVariant = 0;
 constexpr int kDefaultClusterVariant = 0;
 constexpr int kCompensatedTiledVariant = 7;
 constexpr int kMaxSplits = 1024;
-constexpr int64_t kMaxScratchBytes = int64_t(2) << 30;
+constexpr int64_t kDesignBudget = NBODY_DEFAULT_WORKSPACE_BYTES;
 // Relative cost model (only ratios matter): pair rate of one SM, the fixed
 // cost of a work item in source-body equivalents, one launch, scratch traffic.
 constexpr double kPairsPerSmSecond = 1.4e10;
@@ -140,27 +212,45 @@ constexpr double kScratchBytesPerSecond = 5.0e12;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-void plan_tiled(int64_t nt, int64_t ns, int sm, int occ, int variant, int splits_req,
-                nbody_plan *p) {
+// Workspace of the pool-based calls: the default budget, or where n is so
+// large that one group of symmetric partials exceeds it (n above about 20
+// million), the least workspace any symmetric plan needs (3 partial arrays).
+int64_t pool_budget(int64_t n) { return std::max<int64_t>(kDesignBudget, 48 * n); }
+
+// Groups per pass for `groups` groups of `per_group` bytes each within
+// `budget`: all in one pass, or passes plus one carry slot of `carry` bytes.
+// Returns 0 if not even one group fits.
+int64_t groups_per_pass(int64_t groups, int64_t per_group, int64_t carry, int64_t budget) {
+    if (groups * per_group <= budget) return groups;
+    const int64_t g = (budget - carry) / per_group;
+    return g < 1 ? 0 : std::min(g, groups);
+}
+
+int64_t pass_bytes(int64_t groups, int64_t gpp, int64_t per_group, int64_t carry) {
+    return gpp >= groups ? groups * per_group : gpp * per_group + carry;
+}
+
+bool plan_tiled(int64_t nt, int64_t ns, int sm, int occ, int variant, int splits_req,
+                int64_t budget, nbody_plan *p) {
     const nbody::TiledVariant &v = nbody::tiled_variant(variant);
     const int64_t bi = static_cast<int64_t>(v.threads) * v.i_per_thread;
     const int64_t num_ib = ceil_div(nt, bi);
     const int64_t ntiles = ceil_div(ns, v.tile);
     const int64_t slots = static_cast<int64_t>(sm > 0 ? sm : 1) * (occ > 0 ? occ : 1);
     const double slot_rate = kPairsPerSmSecond / (occ > 0 ? occ : 1);
+    const int64_t rec = 16 * nt;   // one partial array
 
+    // decomposition: pieces S within the design budget
     int64_t s_lo = 1, s_hi = std::min<int64_t>(ntiles, kMaxSplits);
-    s_hi = std::max<int64_t>(1, std::min<int64_t>(s_hi, kMaxScratchBytes / (16 * nt)));
+    s_hi = std::max<int64_t>(1, std::min<int64_t>(s_hi, kDesignBudget / rec));
     if (splits_req > 0) s_lo = s_hi = std::min<int64_t>(splits_req, ntiles);
-
     double best_t = INFINITY;
-    int64_t best_s = 1, best_tps = ntiles, best_waves = 1;
+    int64_t best_s = 1, best_tps = ntiles;
     for (int64_t s = s_lo; s <= s_hi; ++s) {
         const int64_t tps = ceil_div(ntiles, s);
         const int64_t used = ceil_div(ntiles, tps);
         if (used != s && splits_req <= 0) continue;   // same as a smaller S
-        const int64_t items = num_ib * used;
-        const int64_t waves = ceil_div(items, slots);
+        const int64_t waves = ceil_div(num_ib * used, slots);
         double t = static_cast<double>(waves) *
                    static_cast<double>(tps * v.tile + kItemOverheadBodies) * bi / slot_rate;
         if (used > 1) t += kLaunchSeconds + 32.0 * used * nt / kScratchBytesPerSecond;
@@ -168,9 +258,20 @@ void plan_tiled(int64_t nt, int64_t ns, int sm, int occ, int variant, int splits
             best_t = t;
             best_s = used;
             best_tps = tps;
-            best_waves = waves;
         }
     }
+    // execution within the workspace
+    int64_t gpp = 1;
+    if (best_s > 1) {
+        gpp = groups_per_pass(best_s, rec, rec, budget);
+        if (gpp == 0) {   // not even one piece and the carry: no partials
+            best_s = 1;
+            best_tps = ntiles;
+            gpp = 1;
+        }
+    }
+    const int64_t passes = ceil_div(best_s, gpp);
+    const int64_t waves = ceil_div(num_ib * gpp, slots);
     p->path = NBODY_PATH_TILED;
     p->variant = variant;
     p->i_per_thread = v.i_per_thread;
@@ -181,9 +282,15 @@ void plan_tiled(int64_t nt, int64_t ns, int sm, int occ, int variant, int splits
     p->tiles_per_split = static_cast<int32_t>(best_tps);
     p->cluster = 1;
     p->warps_j = 1;
-    p->grid = num_ib * best_s;
-    p->scratch_bytes = best_s > 1 ? 16 * best_s * nt : 0;
-    p->fill = static_cast<double>(num_ib * best_s) / static_cast<double>(best_waves * slots);
+    p->dists = 0;
+    p->groups = static_cast<int32_t>(best_s);
+    p->groups_per_pass = static_cast<int32_t>(gpp);
+    p->passes = static_cast<int32_t>(passes);
+    p->grid = num_ib * gpp;
+    p->scratch_bytes = best_s > 1 ? pass_bytes(best_s, gpp, rec, rec) : 0;
+    p->scratch_min_bytes = best_s > 1 ? std::min<int64_t>(best_s, 2) * rec : 0;
+    p->fill = static_cast<double>(num_ib * gpp) / static_cast<double>(waves * slots);
+    return true;
 }
 
 // Small-N path: a cluster of C CTAs (C in 1, 2, 4, 8) shares 32 K targets;
@@ -247,8 +354,13 @@ void plan_cluster_variant(int64_t nt, int64_t ns, int sm, int occ, int variant, 
     p->tiles_per_split = static_cast<int32_t>(best_tpc);
     p->cluster = static_cast<int32_t>(best_c);
     p->warps_j = v.warps;
+    p->dists = 0;
+    p->groups = 1;
+    p->groups_per_pass = 1;
+    p->passes = 1;
     p->grid = num_ib * best_c;
     p->scratch_bytes = 0;
+    p->scratch_min_bytes = 0;
     p->fill = best_fill > 1.0 ? 1.0 : best_fill;
     *t_out = best_t;
 }
@@ -264,86 +376,155 @@ constexpr int64_t kClusterMaxN = 6144;
 // (54.5 against 57.6 us at 10240; 221 against 264 us at 24576), 512-body
 // blocks win up to about 45K bodies (better filled waves), 1024-body blocks
 // up to about 160K, and 2048-body blocks above (fewer partial slots); each
-// choice is within 4.5 % of the fastest shape at every size measured.  The
-// j-side partials take (nb - 1) / 2 (+1) records per body, so they grow as
-// n^2 / T: the cap below bounds them.
+// choice is within 4.5 % of the fastest shape at every size measured.
 constexpr int64_t kSymMinN = 10240;
 constexpr int64_t kSymMidN = 45056;     // from here 1024-body blocks
 constexpr int64_t kSymLargeN = 163840;  // from here 2048-body blocks
 constexpr int kSymSmallVariant = 2;     // K = 8, 2 warps: 512-body blocks
 constexpr int kSymMidVariant = 1;       // K = 8, 4 warps: 1024-body blocks
 constexpr int kDefaultSymVariant = 0;   // K = 8, 8 warps: 2048-body blocks
-constexpr int64_t kMaxSymScratchBytes = int64_t(24) << 30;
 // Relative cost model of the symmetric path: evaluations (two interactions
-// each) per SM-second, the fixed cost of a CTA in evaluations, scratch traffic.
+// each) per SM-second, the fixed cost of a CTA in evaluations.
 constexpr double kSymEvalsPerSmSecond = 1.1e10;
 constexpr double kSymItemOverheadEvals = 64.0 * 1024.0;
 
-struct Occupancy {
-    const int *tiled;
-    const int *cluster;
-    const int *sym;
-};
-
-// Block count, j-side slots per body (the largest), and units per row (the
-// largest) of the symmetric decomposition.
 struct SymGeometry {
-    int64_t block, nb, jslots, units;
+    int64_t block, nb, ndist, spb;
 };
 
 SymGeometry sym_geometry(const nbody::SymVariant &v, int64_t n) {
     SymGeometry g;
     g.block = 32LL * v.warps * v.i_per_thread;
     g.nb = ceil_div(n, g.block);
-    const int64_t h = (g.nb - 1) / 2;
-    g.jslots = h + (g.nb % 2 == 0 ? 1 : 0);
-    g.units = (1 + g.jslots) * (g.block / v.sub);
+    g.ndist = nbody::sym_ndist(static_cast<int>(g.nb));
+    g.spb = g.block / v.sub;
     return g;
 }
 
-bool plan_sym(int64_t n, int sm, int occ, int variant, int splits_req, nbody_plan *p) {
+// Modelled time of the symmetric decomposition (P pieces, D distances per
+// group) run in passes of gpp groups.
+double sym_time(const SymGeometry &g, int64_t n, const nbody::SymVariant &v, int64_t slots,
+                double slot_rate, int64_t P, int64_t D, int64_t js, int64_t gpp) {
+    const int64_t groups = ceil_div(g.ndist, D);
+    const bool reduce = !(g.nb == 1 && P == 1);
+    const int64_t passes = ceil_div(groups, gpp);
+    const double unit_evals = static_cast<double>(g.block) * v.sub;
+    auto pass_time = [&](int64_t gp, int64_t dists_last, bool carry_in, bool carry_out) {
+        const int64_t waves = ceil_div(g.nb * P * gp, slots);
+        // the largest piece: D distances (dists_last in a pass of the last group alone)
+        const int64_t d_big = gp > 1 ? D : dists_last;
+        const int64_t upp = ceil_div(d_big * g.spb, P);
+        double t = static_cast<double>(waves) * (upp * unit_evals + kSymItemOverheadEvals) / slot_rate +
+                   kLaunchSeconds;
+        if (reduce) {
+            const double recs = static_cast<double>(gp * (P + js)) + 1.0 + (carry_in ? 2.0 : 0.0) +
+                                (carry_out ? 1.0 : 0.0);
+            t += kLaunchSeconds + 16.0 * recs * n / kScratchBytesPerSecond;
+        }
+        return t;
+    };
+    const int64_t last_groups = groups - (passes - 1) * gpp;
+    const int64_t dists_last = g.ndist - (groups - 1) * D;
+    double t = 0.0;
+    if (passes > 1) {
+        t += pass_time(gpp, D, false, true);                       // first
+        if (passes > 2) t += (passes - 2) * pass_time(gpp, D, true, true);
+        t += pass_time(last_groups, last_groups > 1 ? D : dists_last, true, false);
+    } else {
+        t = pass_time(groups, groups > 1 ? D : dists_last, false, false);
+    }
+    return t;
+}
+
+// Returns false if the decomposition cannot run within `budget` (a workspace
+// smaller than one group and its carry slot).
+bool plan_sym(int64_t n, int sm, int occ, int variant, int splits_req, int dists_req,
+              int64_t budget, nbody_plan *p) {
     const nbody::SymVariant &v = nbody::sym_variant(variant);
     const SymGeometry g = sym_geometry(v, n);
-    const int64_t jbytes = 16 * g.jslots * n;
-    if (jbytes + 16 * n > kMaxSymScratchBytes) return false;
     const int64_t slots = static_cast<int64_t>(sm > 0 ? sm : 1) * (occ > 0 ? occ : 1);
     const double slot_rate = kSymEvalsPerSmSecond / (occ > 0 ? occ : 1);
-    const double unit_evals = static_cast<double>(g.block) * v.sub;
+    const int64_t rec = 16 * n;
+    // the decomposition is chosen within the design budget (or the least
+    // workspace any decomposition needs, for very large n)
+    const int64_t design = pool_budget(n);
+    const int64_t grid_cap = INT32_MAX;
 
-    // pieces allowed by the partials' cap (each piece adds one i-side slot)
-    const int64_t s_cap = std::max<int64_t>(1, (kMaxSymScratchBytes - jbytes) / (16 * n));
-    int64_t s_lo = 1, s_hi = std::min<int64_t>(std::min<int64_t>(g.units, kMaxSplits), s_cap);
-    if (splits_req > 0) s_lo = s_hi = std::min<int64_t>(std::min<int64_t>(splits_req, g.units), s_cap);
-
-    double best_t = INFINITY;
-    int64_t best_s = 1, best_upp = g.units, best_waves = 1;
-    for (int64_t s = s_lo; s <= s_hi; ++s) {
-        const int64_t upp = ceil_div(g.units, s);   // units of the largest piece
-        const int64_t waves = ceil_div(g.nb * s, slots);
-        double t = static_cast<double>(waves) * (upp * unit_evals + kSymItemOverheadEvals) /
-                   slot_rate;
-        const bool reduce = s > 1 || g.jslots > 0;
-        if (reduce) t += kLaunchSeconds + 16.0 * (s + g.jslots + 1) * n / kScratchBytesPerSecond;
-        if (t < best_t * (1.0 - 1e-3)) {
-            best_t = t;
-            best_s = s;
-            best_upp = upp;
-            best_waves = waves;
+    // distances per group: those giving distinct group counts
+    int64_t dcand[4096];
+    int nd = 0;
+    if (dists_req > 0) {
+        dcand[nd++] = std::min<int64_t>(dists_req, g.ndist);
+    } else {
+        int64_t last = -1;
+        for (int64_t k = 1; k <= g.ndist && nd < 4096; ++k) {
+            const int64_t D = ceil_div(g.ndist, k);
+            if (D != last) dcand[nd++] = D;
+            last = D;
+            if (D == 1) break;
         }
     }
+    double best_t = INFINITY;
+    int64_t best_p = 0, best_d = 0;
+    int64_t p_hi_req = splits_req > 0 ? splits_req : 0;
+    for (;;) {
+        for (int c = 0; c < nd; ++c) {
+            const int64_t D = dcand[c];
+            const int64_t groups = ceil_div(g.ndist, D);
+            const int64_t js = nbody::sym_group_jslots(static_cast<int>(g.nb), static_cast<int>(D));
+            const int64_t p_max = std::max<int64_t>(1, std::min<int64_t>(kMaxSplits, D * g.spb));
+            const int64_t lo = p_hi_req > 0 ? std::min(p_hi_req, p_max) : 1;
+            const int64_t hi = p_hi_req > 0 ? lo : p_max;
+            for (int64_t P = lo; P <= hi; ++P) {
+                const bool reduce = !(g.nb == 1 && P == 1);
+                const int64_t per_group = (P + js) * rec;
+                const int64_t gpp = reduce ? groups_per_pass(groups, per_group, rec, design) : groups;
+                if (gpp == 0 || g.nb * P * gpp > grid_cap) continue;
+                const double t = sym_time(g, n, v, slots, slot_rate, P, D, js, gpp);
+                if (t < best_t * (1.0 - 1e-4)) {
+                    best_t = t;
+                    best_p = P;
+                    best_d = D;
+                }
+            }
+        }
+        if (best_p > 0 || p_hi_req <= 1) break;
+        p_hi_req = p_hi_req / 2;   // a forced piece count too large for the design budget
+    }
+    if (best_p == 0) return false;
+
+    // execution within the workspace
+    const int64_t P = best_p, D = best_d;
+    const int64_t groups = ceil_div(g.ndist, D);
+    const int64_t js = nbody::sym_group_jslots(static_cast<int>(g.nb), static_cast<int>(D));
+    const bool reduce = !(g.nb == 1 && P == 1);
+    const int64_t per_group = (P + js) * rec;
+    int64_t gpp = groups;
+    if (reduce) {
+        gpp = groups_per_pass(groups, per_group, rec, budget);
+        if (gpp == 0) return false;
+        while (g.nb * P * gpp > grid_cap) --gpp;
+    }
+    const int64_t passes = ceil_div(groups, gpp);
+    const int64_t waves = ceil_div(g.nb * P * gpp, slots);
     p->path = NBODY_PATH_SYMMETRIC;
     p->variant = variant;
     p->i_per_thread = v.i_per_thread;
     p->threads = v.warps * 32;
     p->tile = v.sub;
     p->num_iblocks = static_cast<int32_t>(g.nb);
-    p->splits = static_cast<int32_t>(best_s);
-    p->tiles_per_split = static_cast<int32_t>(best_upp);
+    p->splits = static_cast<int32_t>(P);
+    p->tiles_per_split = static_cast<int32_t>(ceil_div(std::min<int64_t>(D, g.ndist) * g.spb, P));
     p->cluster = 1;
     p->warps_j = 1;
-    p->grid = g.nb * best_s;
-    p->scratch_bytes = (best_s > 1 || g.jslots > 0) ? 16 * (best_s + g.jslots) * n : 0;
-    p->fill = static_cast<double>(g.nb * best_s) / static_cast<double>(best_waves * slots);
+    p->dists = static_cast<int32_t>(D);
+    p->groups = static_cast<int32_t>(groups);
+    p->groups_per_pass = static_cast<int32_t>(gpp);
+    p->passes = static_cast<int32_t>(passes);
+    p->grid = g.nb * P * gpp;
+    p->scratch_bytes = reduce ? pass_bytes(groups, gpp, per_group, rec) : 0;
+    p->scratch_min_bytes = reduce ? std::min<int64_t>(groups * per_group, per_group + rec) : 0;
+    p->fill = static_cast<double>(g.nb * P * gpp) / static_cast<double>(waves * slots);
     return true;
 }
 
@@ -351,18 +532,11 @@ int auto_sym_variant(int64_t n) {
     return n < kSymMidN ? kSymSmallVariant : (n < kSymLargeN ? kSymMidVariant : kDefaultSymVariant);
 }
 
-// all_pairs: the targets are the sources (same array, nt == ns), the case the
-// symmetric path needs.
-nbody_status make_plan(int64_t nt, int64_t ns, bool all_pairs, int sm, const Occupancy &occ,
-                       const nbody_forces_opts *opts, nbody_plan *p) {
-    if (nt <= 0 || nt > INT32_MAX || ns <= 0 || ns > INT32_MAX || sm <= 0 || p == nullptr)
-        return NBODY_ERR_INVALID_ARG;
-    nbody_forces_opts o = {NBODY_PATH_AUTO, -1, 0, 0};
-    if (opts != nullptr) o = *opts;
-    if (o.path < NBODY_PATH_AUTO || o.path > NBODY_PATH_SYMMETRIC || o.splits < 0)
-        return NBODY_ERR_INVALID_ARG;
-    if (o.precision < 0 || o.precision > 1) return NBODY_ERR_INVALID_ARG;
-    if (o.precision == 1) {   // compensated: the tiled path's compensated kernel
+nbody_status make_plan_uncached(int64_t nt, int64_t ns, bool all_pairs, int sm,
+                                const Occupancy &occ, const nbody_forces_opts &o_in,
+                                int64_t budget, nbody_plan *p) {
+    nbody_forces_opts o = o_in;
+    if (o.precision == NBODY_PRECISION_COMPENSATED) {   // the tiled path's compensated kernel
         if (o.path == NBODY_PATH_CLUSTER || o.path == NBODY_PATH_SYMMETRIC ||
             (o.variant >= 0 && o.variant != kCompensatedTiledVariant))
             return NBODY_ERR_INVALID_ARG;
@@ -371,13 +545,15 @@ nbody_status make_plan(int64_t nt, int64_t ns, bool all_pairs, int sm, const Occ
     }
     all_pairs = all_pairs && nt == ns;
     if (o.path == NBODY_PATH_SYMMETRIC && !all_pairs) return NBODY_ERR_INVALID_ARG;
+    if (o.dists != 0 && o.path != NBODY_PATH_SYMMETRIC && o.path != NBODY_PATH_AUTO)
+        return NBODY_ERR_INVALID_ARG;
     int path = o.path;
     if (path == NBODY_PATH_AUTO) {
         if (nt <= kClusterMaxN && ns <= kClusterMaxN) {
             path = NBODY_PATH_CLUSTER;
         } else if (all_pairs && nt >= kSymMinN &&
                    plan_sym(nt, sm, occ.sym[auto_sym_variant(nt)], auto_sym_variant(nt), o.splits,
-                            p)) {
+                            o.dists, budget, p)) {
             return NBODY_OK;
         } else {
             path = NBODY_PATH_TILED;
@@ -387,14 +563,15 @@ nbody_status make_plan(int64_t nt, int64_t ns, bool all_pairs, int sm, const Occ
         const int variant = o.variant < 0 ? auto_sym_variant(nt) : o.variant;
         if (variant >= nbody::sym_variant_count() || variant >= kMaxVariants)
             return NBODY_ERR_INVALID_ARG;
-        return plan_sym(nt, sm, occ.sym[variant], variant, o.splits, p) ? NBODY_OK
-                                                                        : NBODY_ERR_INVALID_ARG;
+        return plan_sym(nt, sm, occ.sym[variant], variant, o.splits, o.dists, budget, p)
+                   ? NBODY_OK
+                   : NBODY_ERR_WORKSPACE;
     }
     if (path == NBODY_PATH_TILED) {
         const int variant = o.variant < 0 ? kDefaultTiledVariant : o.variant;
         if (variant >= nbody::tiled_variant_count() || variant >= kMaxVariants)
             return NBODY_ERR_INVALID_ARG;
-        plan_tiled(nt, ns, sm, occ.tiled[variant], variant, o.splits, p);
+        plan_tiled(nt, ns, sm, occ.tiled[variant], variant, o.splits, budget, p);
         return NBODY_OK;
     }
     if (o.splits != 0) return NBODY_ERR_INVALID_ARG;   // the cluster path plans its own split
@@ -404,79 +581,118 @@ nbody_status make_plan(int64_t nt, int64_t ns, bool all_pairs, int sm, const Occ
     // fastest or within a few percent from 1024 to 6144 bodies, so automatic
     // planning uses it and a forced variant is honoured.
     const int only = o.variant >= 0 ? o.variant : kDefaultClusterVariant;
-    double best = INFINITY;
-    for (int v = 0; v < nbody::cluster_variant_count(); ++v) {
-        if (v != only) continue;
-        nbody_plan cand;
-        double t;
-        plan_cluster_variant(nt, ns, sm, occ.cluster[v], v, &cand, &t);
-        if (t < best * (1.0 - 1e-3)) {
-            best = t;
-            *p = cand;
-        }
-    }
+    double t = INFINITY;
+    plan_cluster_variant(nt, ns, sm, occ.cluster[only], only, p, &t);
     // a forced whole-range variant whose range cannot fit shared memory
-    return std::isfinite(best) ? NBODY_OK : NBODY_ERR_INVALID_ARG;
+    return std::isfinite(t) ? NBODY_OK : NBODY_ERR_INVALID_ARG;
 }
 
-// Launch a planned force evaluation; `scratch` holds plan.scratch_bytes when
-// that is not 0.
+// all_pairs: the targets are the sources (same array, nt == ns), the case the
+// symmetric path needs.  `budget`: workspace bytes the plan may use.
+nbody_status make_plan(int64_t nt, int64_t ns, bool all_pairs, int sm, const Occupancy &occ,
+                       const nbody_forces_opts *opts, int64_t budget, nbody_plan *p,
+                       DeviceState *cache = nullptr) {
+    if (nt <= 0 || nt > INT32_MAX || ns <= 0 || ns > INT32_MAX || sm <= 0 || p == nullptr ||
+        budget < 0)
+        return NBODY_ERR_INVALID_ARG;
+    nbody_forces_opts o = {NBODY_PATH_AUTO, -1, 0, NBODY_PRECISION_DEFAULT,
+                           NBODY_QUANTITIES_ACC_POT, 0};
+    if (opts != nullptr) o = *opts;
+    if (o.path < NBODY_PATH_AUTO || o.path > NBODY_PATH_SYMMETRIC || o.splits < 0 || o.dists < 0)
+        return NBODY_ERR_INVALID_ARG;
+    if (o.precision < 0 || o.precision > 1) return NBODY_ERR_INVALID_ARG;
+    if (o.quantities < 0 || o.quantities > 1) return NBODY_ERR_INVALID_ARG;
+    const PlanKey key = {nt, ns, budget, all_pairs ? 1 : 0, sm, o};
+    if (cache != nullptr) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        for (int k = 0; k < cache->plan_count; ++k)
+            if (cache->plan_key[k] == key) {
+                *p = cache->plan_val[k];
+                return NBODY_OK;
+            }
+    }
+    nbody_plan plan = {};
+    const nbody_status st = make_plan_uncached(nt, ns, all_pairs, sm, occ, o, budget, &plan);
+    if (st != NBODY_OK) return st;
+    *p = plan;
+    if (cache != nullptr) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        cache->plan_key[cache->plan_next] = key;
+        cache->plan_val[cache->plan_next] = plan;
+        cache->plan_next = (cache->plan_next + 1) % kPlanCache;
+        cache->plan_count = std::min(cache->plan_count + 1, kPlanCache);
+    }
+    return NBODY_OK;
+}
+
+// ---------------------------------------------------------------- launching
+
+// Launch a planned force evaluation.  `ws` holds plan.scratch_bytes when that
+// is not 0.  With `eu`, the Euler update is applied to every body as its
+// final result is formed when the plan ends in a reduction kernel; *fused
+// tells whether that happened (otherwise the caller launches the update).
 cudaError_t launch_planned(const nbody_plan &plan, const nbody::Problem &pr, float4 *out,
-                           float4 *scratch, int sm_count, cudaStream_t stream) {
+                           void *ws, int sm_count, cudaStream_t stream,
+                           const nbody::EulerFuse *eu = nullptr, bool *fused = nullptr) {
+    if (fused != nullptr) *fused = false;
+    float4 *parts = static_cast<float4 *>(ws);
+    const int64_t nt = pr.nt;
     if (plan.path == NBODY_PATH_SYMMETRIC) {
-        const int block = plan.threads * plan.i_per_thread;
+        nbody::SymLaunch sl = {plan.num_iblocks, plan.splits, plan.dists, 0, 1, 0};
         if (plan.scratch_bytes == 0)   // one block, one piece: no partials
-            return nbody::launch_sym(plan.variant, pr.targets, pr.nt, pr.eps2, plan.num_iblocks, 1,
-                                     out, nullptr, stream);
-        float4 *jpart = scratch + static_cast<int64_t>(plan.splits) * pr.nt;
-        cudaError_t e = nbody::launch_sym(plan.variant, pr.targets, pr.nt, pr.eps2,
-                                          plan.num_iblocks, plan.splits, scratch, jpart, stream);
-        if (e == cudaSuccess)
-            e = nbody::launch_reduce_sym(scratch, plan.splits, jpart, pr.nt, block,
-                                         plan.num_iblocks, out, sm_count, stream);
-        return e;
+            return nbody::launch_sym(plan.variant, pr.targets, pr.nt, pr.eps2, pr.pot, sl, out,
+                                     stream);
+        const int js = nbody::sym_group_jslots(plan.num_iblocks, plan.dists);
+        sl.gstride = static_cast<int64_t>(plan.splits + js) * nt;
+        float4 *lo = parts + static_cast<int64_t>(plan.groups_per_pass) * sl.gstride;
+        for (int pass = 0; pass < plan.passes; ++pass) {
+            sl.g0 = pass * plan.groups_per_pass;
+            sl.groups = std::min(plan.groups_per_pass, plan.groups - sl.g0);
+            cudaError_t e = nbody::launch_sym(plan.variant, pr.targets, pr.nt, pr.eps2, pr.pot, sl,
+                                              parts, stream);
+            if (e != cudaSuccess) return e;
+            const bool last = pass + 1 == plan.passes;
+            const nbody::ReducePass rp = {parts, sl.gstride, plan.splits, true, plan.dists,
+                                          plan.num_iblocks, plan.threads * plan.i_per_thread,
+                                          sl.g0, sl.groups, pr.nt, out, lo, pass > 0, last};
+            e = nbody::launch_reduce_pass(rp, sm_count, stream, last ? eu : nullptr);
+            if (e != cudaSuccess) return e;
+        }
+        if (fused != nullptr) *fused = eu != nullptr;
+        return cudaSuccess;
     }
     const int ntiles = static_cast<int>(ceil_div(pr.ns, plan.tile));
     if (plan.path == NBODY_PATH_CLUSTER)
         return nbody::launch_cluster(plan.variant, pr, plan.num_iblocks, plan.cluster,
                                      plan.tiles_per_split, ntiles, out, stream);
     if (plan.splits == 1)
-        return nbody::launch_tiled(plan.variant, pr, plan.num_iblocks, 1, plan.tiles_per_split,
+        return nbody::launch_tiled(plan.variant, pr, plan.num_iblocks, 0, 1, plan.tiles_per_split,
                                    ntiles, out, stream);
-    cudaError_t e = nbody::launch_tiled(plan.variant, pr, plan.num_iblocks, plan.splits,
-                                        plan.tiles_per_split, ntiles, scratch, stream);
-    if (e == cudaSuccess) e = nbody::launch_reduce_splits(scratch, pr.nt, plan.splits, out, sm_count, stream);
-    return e;
+    float4 *lo = parts + static_cast<int64_t>(plan.groups_per_pass) * nt;
+    for (int pass = 0; pass < plan.passes; ++pass) {
+        const int piece0 = pass * plan.groups_per_pass;
+        const int pieces = std::min(plan.groups_per_pass, plan.splits - piece0);
+        cudaError_t e = nbody::launch_tiled(plan.variant, pr, plan.num_iblocks, piece0, pieces,
+                                            plan.tiles_per_split, ntiles, parts, stream);
+        if (e != cudaSuccess) return e;
+        const bool last = pass + 1 == plan.passes;
+        const nbody::ReducePass rp = {parts, nt, 1, false, 0, 1, 1, piece0, pieces, pr.nt,
+                                      out, lo, pass > 0, last};
+        e = nbody::launch_reduce_pass(rp, sm_count, stream, last ? eu : nullptr);
+        if (e != cudaSuccess) return e;
+    }
+    if (fused != nullptr) *fused = eu != nullptr;
+    return cudaSuccess;
 }
 
-// One time step: the planned force evaluation, then the Euler update.  When
-// the plan ends in a reduction kernel, the update runs inside it, body by
-// body, as each final (a, p) is formed (same arithmetic, one launch and one
-// pass over the bodies fewer); otherwise the Euler kernel follows.
-cudaError_t launch_step(const nbody_plan &plan, const nbody::Problem &pr, float4 *acc,
-                        float4 *scratch, int sm_count, float4 *pos, float4 *vel, float dt,
-                        cudaStream_t stream) {
+// One time step: the planned force evaluation, then the Euler update (inside
+// the last reduction pass where the plan has one, otherwise its own kernel).
+cudaError_t launch_step(const nbody_plan &plan, const nbody::Problem &pr, float4 *acc, void *ws,
+                        int sm_count, float4 *pos, float4 *vel, float dt, cudaStream_t stream) {
     const nbody::EulerFuse eu = {pos, vel, dt};
-    if (plan.path == NBODY_PATH_SYMMETRIC && plan.scratch_bytes > 0) {
-        const int block = plan.threads * plan.i_per_thread;
-        float4 *jpart = scratch + static_cast<int64_t>(plan.splits) * pr.nt;
-        cudaError_t e = nbody::launch_sym(plan.variant, pr.targets, pr.nt, pr.eps2,
-                                          plan.num_iblocks, plan.splits, scratch, jpart, stream);
-        if (e == cudaSuccess)
-            e = nbody::launch_reduce_sym(scratch, plan.splits, jpart, pr.nt, block,
-                                         plan.num_iblocks, acc, sm_count, stream, &eu);
-        return e;
-    }
-    if (plan.path == NBODY_PATH_TILED && plan.splits > 1) {
-        const int ntiles = static_cast<int>(ceil_div(pr.ns, plan.tile));
-        cudaError_t e = nbody::launch_tiled(plan.variant, pr, plan.num_iblocks, plan.splits,
-                                            plan.tiles_per_split, ntiles, scratch, stream);
-        if (e == cudaSuccess)
-            e = nbody::launch_reduce_splits(scratch, pr.nt, plan.splits, acc, sm_count, stream, &eu);
-        return e;
-    }
-    cudaError_t e = launch_planned(plan, pr, acc, scratch, sm_count, stream);
-    if (e == cudaSuccess) e = nbody::launch_euler(pos, vel, acc, pr.nt, dt, sm_count, stream);
+    bool fused = false;
+    cudaError_t e = launch_planned(plan, pr, acc, ws, sm_count, stream, &eu, &fused);
+    if (e == cudaSuccess && !fused) e = nbody::launch_euler(pos, vel, acc, pr.nt, dt, sm_count, stream);
     return e;
 }
 
@@ -484,27 +700,53 @@ Occupancy device_occupancy(const DeviceState *dev) {
     return {dev->tiled_occ, dev->cluster_occ, dev->sym_occ};
 }
 
-// Launch one planned force evaluation (targets x sources) on `stream`, with
-// its split partials in stream-ordered memory from the device's pool.
+bool is_oom(cudaError_t e) { return e == cudaErrorMemoryAllocation; }
+
+// One planned force evaluation (targets x sources) on `stream`.  With a
+// caller's workspace (ws_bytes >= 0) it plans within it and allocates
+// nothing; otherwise it takes the workspace from the device's pool, within
+// the default budget, and re-plans within less if the pool cannot supply it.
 nbody_status run_forces(const nbody::Problem &pr, const nbody_forces_opts *opts, float *result,
-                        cudaStream_t stream) {
+                        void *ws, int64_t ws_bytes, cudaStream_t stream) {
     DeviceState *dev = nullptr;
     nbody_status st = device_state(&dev);
     if (st != NBODY_OK) return st;
     nbody_plan plan;
     const bool all_pairs = pr.targets == pr.sources && pr.nt == pr.ns;
-    if ((st = make_plan(pr.nt, pr.ns, all_pairs, dev->sm_count, device_occupancy(dev), opts,
-                        &plan)) != NBODY_OK)
-        return st;
+    const Occupancy occ = device_occupancy(dev);
     float4 *out = reinterpret_cast<float4 *>(result);
-    void *scratch = nullptr;
     cudaError_t e;
+    if (ws_bytes >= 0) {
+        if ((st = make_plan(pr.nt, pr.ns, all_pairs, dev->sm_count, occ, opts,
+                            ws == nullptr ? 0 : ws_bytes, &plan, dev)) != NBODY_OK)
+            return st;
+        e = launch_planned(plan, pr, out, ws, dev->sm_count, stream);
+        return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
+    }
+    if ((st = make_plan(pr.nt, pr.ns, all_pairs, dev->sm_count, occ, opts, pool_budget(pr.nt),
+                        &plan, dev)) != NBODY_OK)
+        return st;
+    void *scratch = nullptr;
     if (plan.scratch_bytes > 0) {
-        e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.scratch_bytes), dev->pool,
-                                    stream);
+        cudaMemPool_t pool = nullptr;
+        if ((st = device_pool(dev, &pool)) != NBODY_OK) return st;
+        e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.scratch_bytes), pool, stream);
+        // Short of memory: the least workspace of the same decomposition, then none.
+        for (int64_t fallback : {plan.scratch_min_bytes, int64_t(0)}) {
+            if (!is_oom(e)) break;
+            cudaGetLastError();   // clear the allocation failure
+            scratch = nullptr;
+            if ((st = make_plan(pr.nt, pr.ns, all_pairs, dev->sm_count, occ, opts, fallback, &plan,
+                                dev)) != NBODY_OK)
+                return st;
+            e = plan.scratch_bytes > 0
+                    ? cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.scratch_bytes),
+                                              pool, stream)
+                    : cudaSuccess;
+        }
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    e = launch_planned(plan, pr, out, static_cast<float4 *>(scratch), dev->sm_count, stream);
+    e = launch_planned(plan, pr, out, scratch, dev->sm_count, stream);
     if (scratch != nullptr) {
         const cudaError_t ef = cudaFreeAsync(scratch, stream);
         if (e == cudaSuccess) e = ef;
@@ -512,21 +754,36 @@ nbody_status run_forces(const nbody::Problem &pr, const nbody_forces_opts *opts,
     return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
 }
 
+// Workspace a call would take by default on the current device.
+nbody_status default_workspace(int64_t nt, int64_t ns, bool all_pairs,
+                               const nbody_forces_opts *opts, int64_t *bytes) {
+    DeviceState *dev = nullptr;
+    nbody_status st = device_state(&dev);
+    if (st != NBODY_OK) return st;
+    nbody_plan plan;
+    if ((st = make_plan(nt, ns, all_pairs, dev->sm_count, device_occupancy(dev), opts,
+                        pool_budget(nt), &plan, dev)) != NBODY_OK)
+        return st;
+    *bytes = plan.scratch_bytes;
+    return NBODY_OK;
+}
+
 // ---------------------------------------------------------------- multi-step driver
 //
 // One step (forces, then Euler) is captured once into a CUDA graph on an
 // internal stream and replayed `steps` times on the caller's stream, so a
-// step costs one graph launch instead of two or three kernel launches from
-// the host.  Where the forces end in a reduction kernel (the symmetric path,
-// or the tiled path with split sources), the Euler update runs inside it.
-// On the cluster path (small N) a second graph holds two steps whose Euler
-// update is fused into the force kernel, the positions going from pos_mass
-// to a library-owned second buffer and back; steps run in pairs through it,
-// and an odd last step through the one-step graph.  One graph per device is
-// cached, keyed by every argument but the step count; its split scratch (if
-// any) lives as long as the graph.  When the key changes, the old graph is
-// destroyed (deferred until it finishes) and its scratch freed in stream
-// order behind its last launch.
+// step costs one graph launch instead of several kernel launches from the
+// host.  Where the forces end in a reduction kernel, the Euler update runs
+// inside its last pass.  On the cluster path (small N) a second graph holds
+// two steps whose Euler update is fused into the force kernel, the positions
+// going from pos_mass to a second buffer and back; steps run in pairs
+// through it, and an odd last step through the one-step graph.  One graph
+// per device is cached, keyed by every argument but the step count; its
+// workspace (pool memory, or the caller's) lives as long as the graph.  Each
+// call waits on the GPU for the previous one (event `done`), whatever its
+// stream, so two replays never share the workspace at the same time.  When
+// the key changes, the old graph is destroyed and its pool memory freed in
+// stream order behind its last replay.
 
 struct SimKey {
     const float *pm;
@@ -535,10 +792,13 @@ struct SimKey {
     int64_t n;
     float eps2;
     float dt;
+    void *ws;           // the caller's workspace, or nullptr for pool memory
+    int64_t ws_bytes;
     bool operator==(const SimKey &o) const {
         return pm == o.pm && vel == o.vel && acc == o.acc && n == o.n &&
                std::memcmp(&eps2, &o.eps2, sizeof(float)) == 0 &&
-               std::memcmp(&dt, &o.dt, sizeof(float)) == 0;
+               std::memcmp(&dt, &o.dt, sizeof(float)) == 0 && ws == o.ws &&
+               ws_bytes == o.ws_bytes;
     }
 };
 
@@ -547,8 +807,7 @@ struct SimGraph {
     SimKey key = {};
     cudaGraphExec_t exec = nullptr;    // one step: forces (+ reduction), then Euler
     cudaGraphExec_t exec2 = nullptr;   // small N: two steps with Euler fused into the forces
-    void *scratch = nullptr;           // split partials (tiled path)
-    void *pos_b = nullptr;             // second position buffer of the fused steps
+    void *pool_mem = nullptr;          // pool memory of the workspace (nullptr: the caller's)
     cudaEvent_t done = nullptr;        // recorded after the latest replay
 };
 
@@ -565,14 +824,11 @@ nbody_status sim_release(SimGraph &g, cudaStream_t stream) {
             *x = nullptr;
         }
     }
-    if ((g.scratch != nullptr || g.pos_b != nullptr) && g.done != nullptr)
-        cudaStreamWaitEvent(stream, g.done, 0);
-    for (void **b : {&g.scratch, &g.pos_b}) {
-        if (*b != nullptr) {
-            const cudaError_t ef = cudaFreeAsync(*b, stream);
-            if (e == cudaSuccess) e = ef;
-            *b = nullptr;
-        }
+    if (g.pool_mem != nullptr) {
+        if (g.done != nullptr) cudaStreamWaitEvent(stream, g.done, 0);
+        const cudaError_t ef = cudaFreeAsync(g.pool_mem, stream);
+        if (e == cudaSuccess) e = ef;
+        g.pool_mem = nullptr;
     }
     g.valid = false;
     return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
@@ -592,70 +848,144 @@ cudaError_t capture_graph(cudaStream_t cap, Body body, cudaGraphExec_t *exec) {
     return e;
 }
 
+// The plan of one simulation step and the workspace it needs (the plan's
+// partials, then at small n the second position buffer).
+nbody_status sim_plan(DeviceState *dev, int64_t n, int64_t budget, nbody_plan *plan,
+                      int64_t *bytes) {
+    nbody_status st = make_plan(n, n, true, dev->sm_count, device_occupancy(dev), nullptr, budget,
+                                plan, dev);
+    if (st != NBODY_OK) return st;
+    *bytes = plan->scratch_bytes + (plan->path == NBODY_PATH_CLUSTER ? 16 * n : 0);
+    return NBODY_OK;
+}
+
 nbody_status sim_build(int dev_id, DeviceState *dev, const SimKey &k, SimGraph &g,
                        cudaStream_t stream) {
     nbody_plan plan;
-    nbody_status st = make_plan(k.n, k.n, true, dev->sm_count, device_occupancy(dev), nullptr,
-                                &plan);
-    if (st != NBODY_OK) return st;
+    int64_t need = 0;
+    nbody_status st;
     cudaError_t e;
     if (g_capture[dev_id] == nullptr &&
         (e = cudaStreamCreateWithFlags(&g_capture[dev_id], cudaStreamNonBlocking)) != cudaSuccess)
         return cuda_fail(e);
     if (g.done == nullptr && (e = cudaEventCreateWithFlags(&g.done, cudaEventDisableTiming)) != cudaSuccess)
         return cuda_fail(e);
-    void *scratch = nullptr;
-    if (plan.scratch_bytes > 0) {
-        e = cudaMallocFromPoolAsync(&scratch, static_cast<size_t>(plan.scratch_bytes), dev->pool,
-                                    stream);
-        if (e != cudaSuccess) return cuda_fail(e);
+    void *ws = nullptr;          // the plan's partials, then (small n) the second buffer
+    void *pool_mem = nullptr;
+    int64_t room = 0;            // bytes at ws
+    if (k.ws_bytes >= 0) {
+        // the caller's workspace (a null one has no room at all)
+        room = k.ws != nullptr ? k.ws_bytes : 0;
+        if ((st = sim_plan(dev, k.n, room, &plan, &need)) != NBODY_OK) return st;
+        ws = k.ws;
+    } else {
+        if ((st = sim_plan(dev, k.n, pool_budget(k.n), &plan, &need)) != NBODY_OK) return st;
+        if (need > 0) {
+            cudaMemPool_t pool = nullptr;
+            if ((st = device_pool(dev, &pool)) != NBODY_OK) return st;
+            e = cudaMallocFromPoolAsync(&pool_mem, static_cast<size_t>(need), pool, stream);
+            if (is_oom(e)) {   // the least workspace of the same plan, then none
+                cudaGetLastError();
+                pool_mem = nullptr;
+                if ((st = sim_plan(dev, k.n, plan.scratch_min_bytes, &plan, &need)) != NBODY_OK)
+                    return st;
+                e = need > 0 ? cudaMallocFromPoolAsync(&pool_mem, static_cast<size_t>(need), pool,
+                                                       stream)
+                             : cudaSuccess;
+                if (is_oom(e)) {
+                    cudaGetLastError();
+                    pool_mem = nullptr;
+                    if ((st = sim_plan(dev, k.n, 0, &plan, &need)) != NBODY_OK) return st;
+                    e = cudaSuccess;
+                }
+            }
+            if (e != cudaSuccess) return cuda_fail(e);
+            ws = pool_mem;
+            room = pool_mem != nullptr ? need : 0;
+        }
+    }
+    // the first replay waits for the allocation, on whatever stream it runs
+    if ((e = cudaEventRecord(g.done, stream)) != cudaSuccess) {
+        if (pool_mem != nullptr) cudaFreeAsync(pool_mem, stream);
+        return cuda_fail(e);
     }
     const cudaStream_t cap = g_capture[dev_id];
     const int ni = static_cast<int>(k.n);
     float4 *pos = reinterpret_cast<float4 *>(const_cast<float *>(k.pm));
     float4 *vel = reinterpret_cast<float4 *>(k.vel);
     float4 *acc = reinterpret_cast<float4 *>(k.acc);
-    const nbody::Problem pr = {k.pm, k.pm, ni, ni, k.eps2};
+    const nbody::Problem pr = {k.pm, k.pm, ni, ni, k.eps2, true};
+    void *parts = plan.scratch_bytes > 0 ? ws : nullptr;
     cudaGraphExec_t exec = nullptr, exec2 = nullptr;
-    e = capture_graph(cap, [&](cudaStream_t st) {
-        return launch_step(plan, pr, acc, static_cast<float4 *>(scratch), dev->sm_count, pos, vel,
-                           k.dt, st);
+    e = capture_graph(cap, [&](cudaStream_t s) {
+        return launch_step(plan, pr, acc, parts, dev->sm_count, pos, vel, k.dt, s);
     }, &exec);
     // Small N: two steps per replay with the Euler update fused into the
     // cluster kernel, positions alternating between pos_mass and pos_b.
-    void *pos_b = nullptr;
-    if (e == cudaSuccess && plan.path == NBODY_PATH_CLUSTER) {
-        e = cudaMallocFromPoolAsync(&pos_b, static_cast<size_t>(16 * k.n), dev->pool, stream);
-        if (e == cudaSuccess) {
-            float4 *pb = static_cast<float4 *>(pos_b);
-            const nbody::Problem pr_b = {reinterpret_cast<const float *>(pb),
-                                         reinterpret_cast<const float *>(pb), ni, ni, k.eps2};
-            const int ntiles = static_cast<int>(ceil_div(k.n, plan.tile));
-            const nbody::EulerFuse to_b = {pb, vel, k.dt};
-            const nbody::EulerFuse to_a = {pos, vel, k.dt};
-            e = capture_graph(cap, [&](cudaStream_t st) {
-                cudaError_t el = nbody::launch_cluster(plan.variant, pr, plan.num_iblocks,
-                                                       plan.cluster, plan.tiles_per_split, ntiles,
-                                                       acc, st, &to_b);
-                if (el == cudaSuccess)
-                    el = nbody::launch_cluster(plan.variant, pr_b, plan.num_iblocks, plan.cluster,
-                                               plan.tiles_per_split, ntiles, acc, st, &to_a);
-                return el;
-            }, &exec2);
-        }
+    if (e == cudaSuccess && plan.path == NBODY_PATH_CLUSTER && ws != nullptr &&
+        room >= plan.scratch_bytes + 16 * k.n) {
+        float4 *pb = reinterpret_cast<float4 *>(static_cast<char *>(ws) + plan.scratch_bytes);
+        const nbody::Problem pr_b = {reinterpret_cast<const float *>(pb),
+                                     reinterpret_cast<const float *>(pb), ni, ni, k.eps2, true};
+        const int ntiles = static_cast<int>(ceil_div(k.n, plan.tile));
+        const nbody::EulerFuse to_b = {pb, vel, k.dt};
+        const nbody::EulerFuse to_a = {pos, vel, k.dt};
+        e = capture_graph(cap, [&](cudaStream_t s) {
+            cudaError_t el = nbody::launch_cluster(plan.variant, pr, plan.num_iblocks, plan.cluster,
+                                                   plan.tiles_per_split, ntiles, acc, s, &to_b);
+            if (el == cudaSuccess)
+                el = nbody::launch_cluster(plan.variant, pr_b, plan.num_iblocks, plan.cluster,
+                                           plan.tiles_per_split, ntiles, acc, s, &to_a);
+            return el;
+        }, &exec2);
     }
     if (e != cudaSuccess) {
         if (exec != nullptr) cudaGraphExecDestroy(exec);
-        if (scratch != nullptr) cudaFreeAsync(scratch, stream);
-        if (pos_b != nullptr) cudaFreeAsync(pos_b, stream);
+        if (pool_mem != nullptr) cudaFreeAsync(pool_mem, stream);
         return cuda_fail(e);
     }
     g.key = k;
     g.exec = exec;
     g.exec2 = exec2;
-    g.scratch = scratch;
-    g.pos_b = pos_b;
+    g.pool_mem = pool_mem;
     g.valid = true;
+    return NBODY_OK;
+}
+
+nbody_status run_simulate(float *pos_mass, float *vel, float *acc_pot, int64_t n, float eps2,
+                          float dt, int64_t steps, void *ws, int64_t ws_bytes, cudaStream_t stream) {
+    nbody_status st = check_forces(pos_mass, n, eps2, acc_pot);
+    if (st != NBODY_OK) return st;
+    if (steps < 0 || !std::isfinite(dt)) return NBODY_ERR_INVALID_ARG;
+    if (n == 0 || steps == 0) return NBODY_OK;
+    if (vel == nullptr) return NBODY_ERR_INVALID_ARG;
+    if (!aligned16(vel)) return NBODY_ERR_MISALIGNED;
+    if (overlap(vel, pos_mass, 16 * n) || overlap(vel, acc_pot, 16 * n)) return NBODY_ERR_ALIAS;
+    if (ws_bytes >= 0 &&
+        (st = check_workspace(ws, static_cast<size_t>(ws_bytes),
+                              {{pos_mass, 16 * n}, {vel, 16 * n}, {acc_pot, 16 * n}})) != NBODY_OK)
+        return st;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != NBODY_OK) return st;
+    int dev_id = 0;
+    if ((st = current_device(&dev_id)) != NBODY_OK) return st;
+    std::lock_guard<std::mutex> lock(g_sim_mu);
+    SimGraph &g = g_sim[dev_id];
+    const SimKey key = {pos_mass, vel, acc_pot, n, eps2, dt, ws_bytes >= 0 ? ws : nullptr,
+                        ws_bytes >= 0 ? (ws == nullptr ? 0 : ws_bytes) : -1};
+    if (!(g.valid && g.key == key)) {
+        if (g.valid && (st = sim_release(g, stream)) != NBODY_OK) return st;
+        if ((st = sim_build(dev_id, dev, key, g, stream)) != NBODY_OK) return st;
+    }
+    cudaError_t e = cudaStreamWaitEvent(stream, g.done, 0);   // after the previous replay
+    if (e != cudaSuccess) return cuda_fail(e);
+    int64_t left = steps;
+    if (g.exec2 != nullptr)
+        for (; left >= 2; left -= 2)
+            if ((e = cudaGraphLaunch(g.exec2, stream)) != cudaSuccess) return cuda_fail(e);
+    for (; left > 0; --left)
+        if ((e = cudaGraphLaunch(g.exec, stream)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaEventRecord(g.done, stream)) != cudaSuccess) return cuda_fail(e);
     return NBODY_OK;
 }
 
@@ -667,31 +997,8 @@ int nominal_occ(int i_per_thread, int threads) {
     return occ < 1 ? 1 : occ;
 }
 
-}  // namespace
-
-// ======================================================================= C ABI
-
-extern "C" {
-
-const char *nbody_status_string(nbody_status s) {
-    switch (s) {
-        case NBODY_OK: return "NBODY_OK";
-        case NBODY_ERR_INVALID_ARG: return "NBODY_ERR_INVALID_ARG: invalid argument";
-        case NBODY_ERR_MISALIGNED: return "NBODY_ERR_MISALIGNED: body array not 16-byte aligned";
-        case NBODY_ERR_ALIAS: return "NBODY_ERR_ALIAS: output overlaps an input";
-        case NBODY_ERR_CUDA: return "NBODY_ERR_CUDA: CUDA runtime error";
-        case NBODY_ERR_TIMEOUT: return "NBODY_ERR_TIMEOUT: bounded device wait ran out";
-        case NBODY_ERR_DEVICE: return "NBODY_ERR_DEVICE: current device is not sm_103";
-        case NBODY_ERR_TOO_LARGE:
-            return "NBODY_ERR_TOO_LARGE: n exceeds the fixed scratch of nbody_forces_noalloc";
-    }
-    return "NBODY_ERR_UNKNOWN";
-}
-
-int nbody_last_cuda_error(void) { return g_last_cuda_error; }
-
-nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
-                               const nbody_forces_opts *opts, nbody_plan *plan) {
+nbody_status host_plan(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
+                       const nbody_forces_opts *opts, int64_t budget, nbody_plan *plan) {
     int occ[kMaxVariants], cocc[kMaxVariants], socc[kMaxVariants];
     for (int v = 0; v < nbody::tiled_variant_count() && v < kMaxVariants; ++v) {
         const nbody::TiledVariant &tv = nbody::tiled_variant(v);
@@ -706,70 +1013,210 @@ nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
         const int by_smem = static_cast<int>(kSmemPerSm / static_cast<int64_t>(sv.smem + 1024));
         socc[v] = ctas_per_sm > 0 ? ctas_per_sm : std::max(1, std::min(sv.min_ctas, by_smem));
     }
-    return make_plan(n, n, true, sm_count, Occupancy{occ, cocc, socc}, opts, plan);
+    return make_plan(n, n, true, sm_count, Occupancy{occ, cocc, socc}, opts, budget, plan);
 }
 
-nbody_status nbody_forces_ex(const float *pos_mass, int64_t n, float eps2, float *acc_pot,
-                             const nbody_forces_opts *opts, cudaStream_t stream) {
+nbody_forces_opts with_quantities(const nbody_forces_opts *opts, int quantities) {
+    nbody_forces_opts o = {NBODY_PATH_AUTO, -1, 0, NBODY_PRECISION_DEFAULT, quantities, 0};
+    if (opts != nullptr) {
+        o = *opts;
+        if (quantities != NBODY_QUANTITIES_ACC_POT) o.quantities = quantities;
+    }
+    return o;
+}
+
+bool wants_pot(const nbody_forces_opts *opts) {
+    return opts == nullptr || opts->quantities != NBODY_QUANTITIES_ACC;
+}
+
+nbody_status forces_common(const float *pos_mass, int64_t n, float eps2, float *acc_pot,
+                           const nbody_forces_opts *opts, void *ws, int64_t ws_bytes,
+                           cudaStream_t stream) {
     nbody_status st = check_forces(pos_mass, n, eps2, acc_pot);
     if (st != NBODY_OK || n == 0) return st;
-    const nbody::Problem pr = {pos_mass, pos_mass, static_cast<int>(n), static_cast<int>(n), eps2};
-    return run_forces(pr, opts, acc_pot, stream);
+    if (ws_bytes >= 0 &&
+        (st = check_workspace(ws, static_cast<size_t>(ws_bytes),
+                              {{pos_mass, 16 * n}, {acc_pot, 16 * n}})) != NBODY_OK)
+        return st;
+    const nbody::Problem pr = {pos_mass, pos_mass, static_cast<int>(n), static_cast<int>(n), eps2,
+                               wants_pot(opts)};
+    return run_forces(pr, opts, acc_pot, ws, ws_bytes, stream);
 }
 
-nbody_status nbody_forces_ts(const float *targets, int64_t nt, const float *sources, int64_t ns,
-                             float eps2, float *out, cudaStream_t stream) {
+nbody_status forces_ts_common(const float *targets, int64_t nt, const float *sources, int64_t ns,
+                              float eps2, float *out, const nbody_forces_opts *opts, void *ws,
+                              int64_t ws_bytes, cudaStream_t stream) {
     if (check_n(nt) != NBODY_OK || check_n(ns) != NBODY_OK) return NBODY_ERR_INVALID_ARG;
     if (nt == 0) return NBODY_OK;
     if (targets == nullptr || out == nullptr || (ns > 0 && sources == nullptr))
         return NBODY_ERR_INVALID_ARG;
-    if (!std::isfinite(eps2) || !(eps2 >= FLT_MIN)) return NBODY_ERR_INVALID_ARG;
+    if (!eps2_ok(eps2)) return NBODY_ERR_INVALID_ARG;
     if (!aligned16(targets) || !aligned16(out) || (ns > 0 && !aligned16(sources)))
         return NBODY_ERR_MISALIGNED;
     if (overlap(out, targets, 16 * nt)) return NBODY_ERR_ALIAS;
     if (ns > 0 && overlap2(out, 16 * nt, sources, 16 * ns)) return NBODY_ERR_ALIAS;
+    nbody_status st;
+    if (ws_bytes >= 0 &&
+        (st = check_workspace(ws, static_cast<size_t>(ws_bytes),
+                              {{targets, 16 * nt}, {sources, 16 * ns}, {out, 16 * nt}})) != NBODY_OK)
+        return st;
     if (ns == 0) {   // no sources: every sum is empty
         const cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(16 * nt), stream);
         return e == cudaSuccess ? NBODY_OK : cuda_fail(e);
     }
-    const nbody::Problem pr = {targets, sources, static_cast<int>(nt), static_cast<int>(ns), eps2};
-    return run_forces(pr, nullptr, out, stream);
+    const nbody::Problem pr = {targets, sources, static_cast<int>(nt), static_cast<int>(ns), eps2,
+                               wants_pot(opts)};
+    return run_forces(pr, opts, out, ws, ws_bytes, stream);
 }
 
-nbody_status nbody_simulate(float *pos_mass, float *vel, float *acc_pot, int64_t n, float eps2,
-                            float dt, int64_t steps, cudaStream_t stream) {
-    nbody_status st = check_forces(pos_mass, n, eps2, acc_pot);
-    if (st != NBODY_OK) return st;
-    if (steps < 0 || !std::isfinite(dt)) return NBODY_ERR_INVALID_ARG;
-    if (n == 0 || steps == 0) return NBODY_OK;
-    if (vel == nullptr) return NBODY_ERR_INVALID_ARG;
-    if (!aligned16(vel)) return NBODY_ERR_MISALIGNED;
-    if (overlap(vel, pos_mass, 16 * n) || overlap(vel, acc_pot, 16 * n)) return NBODY_ERR_ALIAS;
-    DeviceState *dev = nullptr;
-    if ((st = device_state(&dev)) != NBODY_OK) return st;
-    int dev_id = 0;
-    cudaError_t e = cudaGetDevice(&dev_id);
-    if (e != cudaSuccess) return cuda_fail(e);
-    std::lock_guard<std::mutex> lock(g_sim_mu);
-    SimGraph &g = g_sim[dev_id];
-    const SimKey key = {pos_mass, vel, acc_pot, n, eps2, dt};
-    if (!(g.valid && g.key == key)) {
-        if (g.valid && (st = sim_release(g, stream)) != NBODY_OK) return st;
-        if ((st = sim_build(dev_id, dev, key, g, stream)) != NBODY_OK) return st;
+}  // namespace
+
+namespace nbody {
+void record_cuda_error(int e) { g_last_cuda_error = e; }
+}  // namespace nbody
+
+// ======================================================================= C ABI
+
+extern "C" {
+
+const char *nbody_status_string(nbody_status s) {
+    switch (s) {
+        case NBODY_OK: return "NBODY_OK";
+        case NBODY_ERR_INVALID_ARG: return "NBODY_ERR_INVALID_ARG: invalid argument";
+        case NBODY_ERR_MISALIGNED: return "NBODY_ERR_MISALIGNED: array not 16-byte aligned";
+        case NBODY_ERR_ALIAS: return "NBODY_ERR_ALIAS: output or workspace overlaps another array";
+        case NBODY_ERR_CUDA: return "NBODY_ERR_CUDA: CUDA runtime error";
+        case NBODY_ERR_TIMEOUT: return "NBODY_ERR_TIMEOUT: bounded device wait ran out";
+        case NBODY_ERR_DEVICE: return "NBODY_ERR_DEVICE: current device is not sm_103";
+        case NBODY_ERR_TOO_LARGE:
+            return "NBODY_ERR_TOO_LARGE: n exceeds the fixed scratch of nbody_forces_noalloc";
+        case NBODY_ERR_WORKSPACE:
+            return "NBODY_ERR_WORKSPACE: the forced path cannot run within the given workspace";
     }
-    int64_t left = steps;
-    if (g.exec2 != nullptr)
-        for (; left >= 2; left -= 2)
-            if ((e = cudaGraphLaunch(g.exec2, stream)) != cudaSuccess) return cuda_fail(e);
-    for (; left > 0; --left)
-        if ((e = cudaGraphLaunch(g.exec, stream)) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaEventRecord(g.done, stream)) != cudaSuccess) return cuda_fail(e);
-    return NBODY_OK;
+    return "NBODY_ERR_UNKNOWN";
+}
+
+int nbody_last_cuda_error(void) { return g_last_cuda_error; }
+
+nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
+                               const nbody_forces_opts *opts, nbody_plan *plan) {
+    return host_plan(n, sm_count, ctas_per_sm, opts, n > 0 ? pool_budget(n) : 0, plan);
+}
+
+nbody_status nbody_plan_forces_ws(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
+                                  const nbody_forces_opts *opts, int64_t workspace_bytes,
+                                  nbody_plan *plan) {
+    if (workspace_bytes < 0) return NBODY_ERR_INVALID_ARG;
+    return host_plan(n, sm_count, ctas_per_sm, opts, workspace_bytes, plan);
+}
+
+nbody_status nbody_forces_ex(const float *pos_mass, int64_t n, float eps2, float *acc_pot,
+                             const nbody_forces_opts *opts, cudaStream_t stream) {
+    return forces_common(pos_mass, n, eps2, acc_pot, opts, nullptr, -1, stream);
 }
 
 nbody_status nbody_forces(const float *pos_mass, int64_t n, float eps2, float *acc_pot,
                           cudaStream_t stream) {
-    return nbody_forces_ex(pos_mass, n, eps2, acc_pot, nullptr, stream);
+    return forces_common(pos_mass, n, eps2, acc_pot, nullptr, nullptr, -1, stream);
+}
+
+nbody_status nbody_forces_acc(const float *pos_mass, int64_t n, float eps2, float *acc_pot,
+                              cudaStream_t stream) {
+    const nbody_forces_opts o = with_quantities(nullptr, NBODY_QUANTITIES_ACC);
+    return forces_common(pos_mass, n, eps2, acc_pot, &o, nullptr, -1, stream);
+}
+
+nbody_status nbody_forces_ts(const float *targets, int64_t nt, const float *sources, int64_t ns,
+                             float eps2, float *out, cudaStream_t stream) {
+    return forces_ts_common(targets, nt, sources, ns, eps2, out, nullptr, nullptr, -1, stream);
+}
+
+nbody_status nbody_forces_ws(const float *pos_mass, int64_t n, float eps2, float *acc_pot,
+                             const nbody_forces_opts *opts, void *workspace,
+                             size_t *workspace_bytes, cudaStream_t stream) {
+    if (workspace_bytes == nullptr) return NBODY_ERR_INVALID_ARG;
+    if (workspace == nullptr) {   // size query
+        if (check_n(n) != NBODY_OK || !eps2_ok(eps2)) return NBODY_ERR_INVALID_ARG;
+        int64_t b = 0;
+        nbody_status st = n == 0 ? NBODY_OK : default_workspace(n, n, true, opts, &b);
+        if (st == NBODY_OK) *workspace_bytes = static_cast<size_t>(b);
+        return st;
+    }
+    if (*workspace_bytes > static_cast<size_t>(INT64_MAX)) return NBODY_ERR_INVALID_ARG;
+    return forces_common(pos_mass, n, eps2, acc_pot, opts, workspace,
+                         static_cast<int64_t>(*workspace_bytes), stream);
+}
+
+nbody_status nbody_forces_ts_ws(const float *targets, int64_t nt, const float *sources,
+                                int64_t ns, float eps2, float *out,
+                                const nbody_forces_opts *opts, void *workspace,
+                                size_t *workspace_bytes, cudaStream_t stream) {
+    if (workspace_bytes == nullptr) return NBODY_ERR_INVALID_ARG;
+    if (workspace == nullptr) {   // size query
+        if (check_n(nt) != NBODY_OK || check_n(ns) != NBODY_OK || !eps2_ok(eps2))
+            return NBODY_ERR_INVALID_ARG;
+        int64_t b = 0;
+        nbody_status st = NBODY_OK;
+        if (nt > 0 && ns > 0)
+            st = default_workspace(nt, ns, targets != nullptr && targets == sources, opts, &b);
+        if (st == NBODY_OK) *workspace_bytes = static_cast<size_t>(b);
+        return st;
+    }
+    if (*workspace_bytes > static_cast<size_t>(INT64_MAX)) return NBODY_ERR_INVALID_ARG;
+    return forces_ts_common(targets, nt, sources, ns, eps2, out, opts, workspace,
+                            static_cast<int64_t>(*workspace_bytes), stream);
+}
+
+nbody_status nbody_simulate(float *pos_mass, float *vel, float *acc_pot, int64_t n, float eps2,
+                            float dt, int64_t steps, cudaStream_t stream) {
+    return run_simulate(pos_mass, vel, acc_pot, n, eps2, dt, steps, nullptr, -1, stream);
+}
+
+nbody_status nbody_simulate_ws(float *pos_mass, float *vel, float *acc_pot, int64_t n,
+                               float eps2, float dt, int64_t steps, void *workspace,
+                               size_t *workspace_bytes, cudaStream_t stream) {
+    if (workspace_bytes == nullptr) return NBODY_ERR_INVALID_ARG;
+    if (workspace == nullptr) {   // size query
+        if (check_n(n) != NBODY_OK || !eps2_ok(eps2)) return NBODY_ERR_INVALID_ARG;
+        if (n == 0) {
+            *workspace_bytes = 0;
+            return NBODY_OK;
+        }
+        DeviceState *dev = nullptr;
+        nbody_status st = device_state(&dev);
+        if (st != NBODY_OK) return st;
+        nbody_plan plan;
+        int64_t need = 0;
+        if ((st = sim_plan(dev, n, pool_budget(n), &plan, &need)) != NBODY_OK) return st;
+        *workspace_bytes = static_cast<size_t>(need);
+        return NBODY_OK;
+    }
+    if (*workspace_bytes > static_cast<size_t>(INT64_MAX)) return NBODY_ERR_INVALID_ARG;
+    return run_simulate(pos_mass, vel, acc_pot, n, eps2, dt, steps, workspace,
+                        static_cast<int64_t>(*workspace_bytes), stream);
+}
+
+nbody_status nbody_release_cached(void) {
+    int dev_id = 0;
+    nbody_status st = current_device(&dev_id);
+    if (st != NBODY_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    {
+        std::lock_guard<std::mutex> lock(g_sim_mu);
+        SimGraph &g = g_sim[dev_id];
+        if (g.valid || g.pool_mem != nullptr) {
+            if ((st = sim_release(g, 0)) != NBODY_OK) return st;
+            if ((e = cudaStreamSynchronize(0)) != cudaSuccess) return cuda_fail(e);
+        }
+    }
+    cudaMemPool_t pool = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        pool = g_dev[dev_id].pool;
+    }
+    if (pool != nullptr && (e = cudaMemPoolTrimTo(pool, 0)) != cudaSuccess) return cuda_fail(e);
+    return NBODY_OK;
 }
 
 nbody_status nbody_euler_step(float *pos_mass, float *vel, const float *acc_pot, int64_t n,

@@ -14,6 +14,7 @@ struct Problem {
     int nt;
     int ns;
     float eps2;
+    bool pot;               // compute the potential (false: .w of every result is 0)
 };
 
 // A compiled instantiation of the tiled force kernel.
@@ -22,15 +23,17 @@ struct TiledVariant {
     int threads;        // threads per CTA
     int tile;           // source bodies per shared-memory tile
     const void *fn_pot; // kernel computing a and p
+    const void *fn_acc; // kernel computing a only
 };
 
 int tiled_variant_count();
 const TiledVariant &tiled_variant(int v);
 
-// Force kernel over grid = num_ib * splits CTAs; CTA b handles i-block
+// Force kernel over grid = num_ib * pieces CTAs; CTA b handles i-block
 // b % num_ib and source tiles [s * tps, min((s + 1) * tps, ntiles)) with
-// s = b / num_ib.  Writes out[s * nt + i] (out = the result when splits == 1).
-cudaError_t launch_tiled(int variant, const Problem &pr, int num_ib, int splits,
+// s = piece0 + b / num_ib.  Writes out[(b / num_ib) * nt + i] (out = the
+// result when the whole source range is one piece).
+cudaError_t launch_tiled(int variant, const Problem &pr, int num_ib, int piece0, int pieces,
                          int tiles_per_split, int ntiles, float4 *out, cudaStream_t stream);
 
 // Euler update applied by a kernel as it stores each body's result:
@@ -51,6 +54,7 @@ struct ClusterVariant {
     int tile;           // source bodies per shared-memory tile
     bool whole;         // stages the CTA's whole source range at once (dynamic smem)
     const void *fn_pot;
+    const void *fn_acc;
 };
 
 // Dynamic shared memory a whole-range cluster launch needs.
@@ -77,31 +81,75 @@ struct SymVariant {
     int sub;            // sources per unit (a barrier and a j-side write-back per unit)
     int min_ctas;       // resident CTAs per SM the register allocation was bounded for
     size_t smem;        // dynamic shared memory per CTA
-    const void *fn;
+    const void *fn_pot;
+    const void *fn_acc;
 };
 
 int sym_variant_count();
 const SymVariant &sym_variant(int v);
 
-// Symmetric kernel over grid = nb * splits CTAs, nb = ceil(n / T): CTA b
-// takes row b % nb, piece b / nb of that row's units.  Writes the i-side
-// partials ipart[piece * n + i] and the j-side partials jpart[(d - 1) * n + j].
-cudaError_t launch_sym(int variant, const float *bodies, int n, float eps2, int nb, int splits,
-                       float4 *ipart, float4 *jpart, cudaStream_t stream);
+// The symmetric decomposition of n bodies into nb blocks of T: block row I
+// evaluates, both ways, the blocks at circular distance d = 1 .. H from it
+// (H = (nb - 1) / 2), and d = nb / 2 as well for I < nb / 2 when nb is even;
+// d = 0 is its own block, evaluated one way.  Distances 0 .. ndist - 1 are
+// taken in groups of D; in each group a row's units (SUB sources of one
+// block) are cut into P pieces.
+struct SymLaunch {
+    int nb;         // blocks
+    int P;          // pieces per row per group
+    int D;          // distances per group
+    int g0;         // first group of this launch
+    int groups;     // groups of this launch: grid = nb * P * groups CTAs
+    int64_t gstride;// records between the partial slots of consecutive groups
+};
 
-// out[i] = the splits i-side slots of body i, then its j-side slots, in a
-// fixed order, compensated (block = T bodies).  With `euler`, each body's
-// Euler step follows in place (euler->pos_out = the positions the force
-// kernel read, which it has finished reading).
-cudaError_t launch_reduce_sym(const float4 *ipart, int splits, const float4 *jpart, int n,
-                              int block, int nb, float4 *out, int sm_count, cudaStream_t stream,
-                              const EulerFuse *euler = nullptr);
+// Distances of the decomposition: 0 .. ndist - 1.
+__host__ __device__ inline int sym_ndist(int nb) {
+    return (nb - 1) / 2 + 1 + (nb % 2 == 0 ? 1 : 0);
+}
 
-// out[i] = sum over s of part[s * n + i], in the order s = 0, 1, ..., compensated;
-// with `euler`, each body's Euler step follows in place, as above.
-cudaError_t launch_reduce_splits(const float4 *part, int n, int splits, float4 *out,
-                                 int sm_count, cudaStream_t stream,
-                                 const EulerFuse *euler = nullptr);
+// The largest j-side slot count of any group (the slot layout's stride is
+// P + that many records per body).
+int sym_group_jslots(int nb, int D);
+
+// Symmetric kernel: CTA b takes row b % nb, piece (b / nb) % P of group
+// g0 + b / (nb P).  Writes the group's i-side partials to
+// parts[gl * gstride + piece * n + i] and its j-side partials to
+// parts[gl * gstride + (P + d - max(dlo, 1)) * n + j] (gl = group - g0, dlo
+// = the group's first distance).  With nb == 1 and P == 1, parts may be the
+// result itself.
+cudaError_t launch_sym(int variant, const float *bodies, int n, float eps2, bool pot,
+                       const SymLaunch &sl, float4 *parts, cudaStream_t stream);
+
+// One pass of the fixed-order compensated reduction.  For every body i, in
+// this order: the running total carried in from the previous pass (its high
+// part in out[i], its low part in lo[i]); then, for each group of the pass,
+// its i-side slots 0 .. islots - 1 and (symmetric path) the j-side slots of
+// the group's distances that reach the body's block, in increasing distance.
+// A final pass stores high - low (and applies `euler` if given); any other
+// stores the high and low parts for the next pass.
+struct ReducePass {
+    const float4 *parts;
+    int64_t gstride;    // records between the slots of consecutive groups
+    int islots;         // i-side slots per group (tiled path: 1)
+    bool sym;           // symmetric path: j-side slots follow the i-side ones
+    int D;              // symmetric: distances per group
+    int nb;             // symmetric: blocks
+    int block;          // symmetric: bodies per block
+    int g0;             // first group of the pass
+    int groups;         // groups in the pass
+    int n;
+    float4 *out;
+    float4 *lo;
+    bool carry_in;
+    bool final_pass;
+};
+
+cudaError_t launch_reduce_pass(const ReducePass &rp, int sm_count, cudaStream_t stream,
+                               const EulerFuse *euler = nullptr);
+
+// Record a CUDA error for nbody_last_cuda_error (this host thread).
+void record_cuda_error(int e);
 
 cudaError_t launch_euler(float4 *pos_mass, float4 *vel, const float4 *acc_pot, int n,
                          float dt, int sm_count, cudaStream_t stream);

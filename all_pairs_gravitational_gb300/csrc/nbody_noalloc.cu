@@ -49,7 +49,12 @@ struct NoAllocDevice {
 std::mutex g_mu;
 NoAllocDevice g_dev[kMaxDevices];
 
-nbody_status fail(cudaError_t) { return NBODY_ERR_CUDA; }
+// Record the CUDA error for nbody_last_cuda_error (defined with the other
+// entry points) and report it.
+nbody_status fail(cudaError_t e) {
+    nbody::record_cuda_error(static_cast<int>(e));
+    return NBODY_ERR_CUDA;
+}
 
 // Per-device set-up, with that device current: no allocation of any kind.
 nbody_status setup(NoAllocDevice **out) {
@@ -109,7 +114,8 @@ extern "C" nbody_status nbody_forces_noalloc(const float *pos_mass, int64_t n, f
     nbody_plan best = {};
     bool have = false;
     for (int64_t s = 1; s <= s_max; ++s) {
-        nbody_forces_opts opts = {NBODY_PATH_TILED, -1, static_cast<int32_t>(s), 0};
+        nbody_forces_opts opts = {NBODY_PATH_TILED, -1, static_cast<int32_t>(s),
+                                  NBODY_PRECISION_DEFAULT, NBODY_QUANTITIES_ACC_POT, 0};
         nbody_plan p;
         if (nbody_plan_forces(n, dev->sm_count, dev->occ, &opts, &p) != NBODY_OK) continue;
         if (p.splits > s_max) continue;
@@ -123,17 +129,19 @@ extern "C" nbody_status nbody_forces_noalloc(const float *pos_mass, int64_t n, f
     const int ni = static_cast<int>(n);
     const int ntiles = static_cast<int>((n + best.tile - 1) / best.tile);
     float4 *out = reinterpret_cast<float4 *>(acc_pot);
-    const nbody::Problem pr = {pos_mass, pos_mass, ni, ni, eps2};
+    const nbody::Problem pr = {pos_mass, pos_mass, ni, ni, eps2, true};
     cudaError_t e;
     if (best.splits == 1) {
-        e = nbody::launch_tiled(best.variant, pr, best.num_iblocks, 1, best.tiles_per_split,
+        e = nbody::launch_tiled(best.variant, pr, best.num_iblocks, 0, 1, best.tiles_per_split,
                                 ntiles, out, stream);
     } else {
-        e = nbody::launch_tiled(best.variant, pr, best.num_iblocks, best.splits,
+        // every piece in one launch, their partials in the fixed array, then
+        // one reduction pass that adds them in piece order
+        e = nbody::launch_tiled(best.variant, pr, best.num_iblocks, 0, best.splits,
                                 best.tiles_per_split, ntiles, dev->scratch, stream);
-        if (e == cudaSuccess)
-            e = nbody::launch_reduce_splits(dev->scratch, ni, best.splits, out, dev->sm_count,
-                                            stream);
+        const nbody::ReducePass rp = {dev->scratch, n, 1, false, 0, 1, 1, 0, best.splits, ni,
+                                      out, nullptr, false, true};
+        if (e == cudaSuccess) e = nbody::launch_reduce_pass(rp, dev->sm_count, stream);
     }
     return e == cudaSuccess ? NBODY_OK : fail(e);
 }

@@ -76,7 +76,8 @@ int main(void) {
 
     /* the symmetric path forced through the options struct, and the planner's
      * automatic choice at 2^20 bodies, from C */
-    nbody_forces_opts opts = {NBODY_PATH_SYMMETRIC, -1, 0, NBODY_PRECISION_DEFAULT};
+    nbody_forces_opts opts = {NBODY_PATH_SYMMETRIC, -1, 0, NBODY_PRECISION_DEFAULT,
+                              NBODY_QUANTITIES_ACC_POT, 0};
     static float acc_sym[N * 4];
     if ((st = nbody_forces_ex(d_pm, N, EPS2, d_vel, &opts, 0)) != NBODY_OK) return 10;
     cudaMemcpy(acc_sym, d_vel, sizeof acc_sym, cudaMemcpyDeviceToHost);
@@ -94,9 +95,28 @@ int main(void) {
     printf("symmetric path from C: worst per-body difference %.3e\n", worst_sym);
     if (!(worst_sym <= 2e-4)) return 11;
     nbody_plan plan;
-    nbody_forces_opts autoo = {NBODY_PATH_AUTO, -1, 0, NBODY_PRECISION_DEFAULT};
+    nbody_forces_opts autoo = {NBODY_PATH_AUTO, -1, 0, NBODY_PRECISION_DEFAULT,
+                              NBODY_QUANTITIES_ACC_POT, 0};
     if (nbody_plan_forces(1 << 20, 152, 0, &autoo, &plan) != NBODY_OK) return 12;
-    if (plan.path != NBODY_PATH_SYMMETRIC || plan.scratch_bytes <= 0) return 13;
+    if (plan.path != NBODY_PATH_SYMMETRIC || plan.scratch_bytes <= 0 ||
+        plan.scratch_bytes > NBODY_DEFAULT_WORKSPACE_BYTES)
+        return 13;
+
+    /* the symmetric path again within a caller-owned workspace: ask for its
+     * size, give it exactly that, and get the same bits */
+    size_t ws_bytes = 0;
+    if (nbody_forces_ws(NULL, N, EPS2, NULL, &opts, NULL, &ws_bytes, 0) != NBODY_OK) return 14;
+    void *ws = NULL;
+    if (ws_bytes > 0 && cudaMalloc(&ws, ws_bytes) != cudaSuccess) return 15;
+    if (nbody_forces_ws(d_pm, N, EPS2, d_vel, &opts, ws ? ws : (void *)d_vel, &ws_bytes, 0) != NBODY_OK)
+        return 16;
+    static float acc_ws[N * 4];
+    cudaMemcpy(acc_ws, d_vel, sizeof acc_ws, cudaMemcpyDeviceToHost);
+    cudaMemcpy(d_vel, vel, sizeof vel, cudaMemcpyHostToDevice);         /* restore */
+    for (int k = 0; k < N * 4; ++k)
+        if (acc_ws[k] != acc_sym[k]) return 17;
+    if (ws) cudaFree(ws);
+    printf("nbody_forces_ws from C: %zu bytes of workspace, same bits\n", ws_bytes);
 
     /* one Euler step, then the same step through nbody_simulate on a copy */
     cudaMemcpy(pm2, d_pm, sizeof pm2, cudaMemcpyDeviceToHost);
@@ -114,6 +134,7 @@ int main(void) {
     for (int k = 0; k < N * 4; ++k)
         if (a1[k] != a2[k]) return 8;
     if (cudaDeviceSynchronize() != cudaSuccess) return 9;
+    if (nbody_release_cached() != NBODY_OK) return 18;
     printf("nbody_euler_step and nbody_simulate agree bit for bit\n");
     return 0;
 }

@@ -128,18 +128,28 @@ def test_euler_argument_checks(lib):
     assert call(a, b, a, 5, 1e-3) == 3            # acc is pos
 
 
-def _covers(plan, n):
+def _covers(plan, n, budget=None):
     """Every target in exactly one target block, every source tile in exactly
-    one piece of the source range."""
+    one piece of the source range, and the workspace within the budget."""
     ntiles = -(-n // plan["tile"])
+    if budget is not None and plan["scratch_min_bytes"] <= budget:
+        assert plan["scratch_bytes"] <= budget
     if plan["path"] == apg.NBODY_PATH_SYMMETRIC:
         _sym_covers(plan, n)
         return
     if plan["path"] == apg.NBODY_PATH_TILED:
         bi = plan["threads"] * plan["i_per_thread"]
         tps, s = plan["tiles_per_split"], plan["splits"]
-        assert plan["grid"] == plan["num_iblocks"] * s
-        assert plan["scratch_bytes"] == (16 * s * n if s > 1 else 0)
+        g, passes = plan["groups_per_pass"], plan["passes"]
+        assert plan["groups"] == s and 1 <= g <= s and passes == -(-s // g)
+        assert plan["grid"] == plan["num_iblocks"] * g
+        rec = 16 * n
+        if s == 1:
+            assert plan["scratch_bytes"] == plan["scratch_min_bytes"] == 0
+        elif passes == 1:
+            assert plan["scratch_bytes"] == s * rec and plan["scratch_min_bytes"] == min(s, 2) * rec
+        else:   # g pieces and the carry slot
+            assert plan["scratch_bytes"] == (g + 1) * rec and plan["scratch_min_bytes"] == 2 * rec
     else:
         assert plan["path"] == apg.NBODY_PATH_CLUSTER
         bi = 32 * plan["i_per_thread"]
@@ -149,7 +159,7 @@ def _covers(plan, n):
         assert plan["threads"] == 32 * plan["warps_j"]
         assert plan["tile"] % plan["warps_j"] == 0 and plan["tile"] // plan["warps_j"] <= 32
         assert plan["grid"] == plan["num_iblocks"] * s
-        assert plan["scratch_bytes"] == 0
+        assert plan["scratch_bytes"] == 0 and plan["passes"] == 1
     assert plan["num_iblocks"] * bi >= n > (plan["num_iblocks"] - 1) * bi
     assert s * tps >= ntiles > (s - 1) * tps
     assert plan["grid"] < 2 ** 31
@@ -169,6 +179,17 @@ def _sym_units(nb):
     return rows
 
 
+def _ndist(nb):
+    return (nb - 1) // 2 + 1 + (1 if nb % 2 == 0 else 0)
+
+
+def _jslots(nb, d_per_group):
+    nd = _ndist(nb)
+    groups = -(-nd // d_per_group)
+    return max(min((g + 1) * d_per_group, nd) - max(g * d_per_group, 1)
+               for g in range(min(groups, 2)))
+
+
 @pytest.mark.parametrize("nb", list(range(1, 40)) + [64, 127, 128, 512, 513])
 def test_symmetric_decomposition_meets_every_pair_once(nb):
     seen = {}
@@ -181,30 +202,102 @@ def test_symmetric_decomposition_meets_every_pair_once(nb):
                 for key in ((i, j), (j, i)):           # one evaluation, both ways
                     seen[key] = seen.get(key, 0) + 1
     assert len(seen) == nb * nb and set(seen.values()) == {1}
-    # j-side slot d - 1 of every body is written by exactly one row
-    slots = {}
-    for row in _sym_units(nb):
-        for i, j, d in row:
-            if d:
-                slots[(j, d - 1)] = slots.get((j, d - 1), 0) + 1
-    assert set(slots.values()) <= {1}
+
+
+def _simulate_slots(nb, spb, P, D, gpp):
+    """The slot traffic of the symmetric path, restated from the header and
+    the kernels' index rules at unit granularity (a unit = spb-th of a
+    block): which (group, slot, block, unit) record each CTA writes, and
+    which records the reduction pass reads for each body's block.  Returns
+    the ordered block pairs each block's final sum covers, with the count."""
+    nd = _ndist(nb)
     h = (nb - 1) // 2
-    for j in range(nb):
-        want = h + (1 if nb % 2 == 0 and j >= nb // 2 else 0)
-        assert sorted(s for (b, s) in slots if b == j) == list(range(want))
+    groups = -(-nd // D)
+    covered = {x: {} for x in range(nb)}
+    for g0 in range(0, groups, gpp):
+        gp = min(gpp, groups - g0)
+        written = {}   # (gl, slot, block, unit) -> (source block set of the partial)
+        for gl in range(gp):
+            dlo = (g0 + gl) * D
+            jbase = max(dlo, 1)
+            for row in range(nb):
+                dmax = h + (1 if nb % 2 == 0 and row < nb // 2 else 0)
+                dhi = min(dlo + D, dmax + 1)
+                units = max(0, dhi - dlo) * spb
+                for piece in range(P):
+                    u0, u1 = units * piece // P, units * (piece + 1) // P
+                    # the i-side slot `piece` of every unit of the row's block
+                    for ub in range(spb):
+                        key = (gl, piece, row, ub)
+                        assert key not in written
+                        written[key] = []
+                    for u in range(u0, u1):
+                        d = dlo + u // spb
+                        sub = u % spb
+                        jblk = (row + d) % nb
+                        for ub in range(spb):     # the row's targets meet unit `sub` of J
+                            written[(gl, piece, row, ub)].append((jblk, sub))
+                        if d != 0:                # unit `sub` of J meets all the row's targets
+                            key = (gl, P + d - jbase, jblk, sub)
+                            assert key not in written, key
+                            written[key] = [(row, ub) for ub in range(spb)]
+        # the reduction pass
+        for x in range(nb):
+            upper = nb % 2 == 0 and x >= nb // 2
+            for ub in range(spb):
+                for gl in range(gp):
+                    dlo = (g0 + gl) * D
+                    jbase = max(dlo, 1)
+                    reads = list(range(P))
+                    dhi = min(dlo + D, nd)
+                    if nb % 2 == 0 and not upper:
+                        dhi = min(dhi, h + 1)
+                    reads += [P + d - jbase for d in range(jbase, dhi)]
+                    for slot in reads:
+                        assert slot < P + _jslots(nb, D)
+                        for src in written[(gl, slot, x, ub)]:
+                            covered[x][(ub, src)] = covered[x].get((ub, src), 0) + 1
+    return covered
+
+
+@pytest.mark.parametrize("nb", [1, 2, 3, 4, 5, 6, 7, 8, 11, 16, 17])
+@pytest.mark.parametrize("P,D", [(1, 1), (1, 2), (2, 1), (3, 2), (4, 3), (5, 7), (2, 64)])
+@pytest.mark.parametrize("gpp", [1, 2, 3, 100])
+def test_symmetric_groups_and_passes_cover_every_pair_once(nb, P, D, gpp):
+    """Every (target unit, source unit) pair reaches the target's final sum
+    exactly once, whatever the pieces, the distances per group and the
+    groups per pass; no partial record is written twice in a pass, and every
+    record the reduction reads was written in that pass."""
+    spb = 3
+    D = min(D, _ndist(nb))
+    covered = _simulate_slots(nb, spb, P, D, gpp)
+    every = {(ub, (j, us)) for ub in range(spb) for j in range(nb) for us in range(spb)}
+    for x in range(nb):
+        assert set(covered[x]) == every and set(covered[x].values()) == {1}, x
 
 
 def _sym_covers(plan, n):
     t = plan["threads"] * plan["i_per_thread"]
     nb = plan["num_iblocks"]
     assert nb == -(-n // t) and t % plan["tile"] == 0 and plan["tile"] % 32 == 0
-    jslots = (nb - 1) // 2 + (1 if nb % 2 == 0 else 0)
-    units = (1 + jslots) * (t // plan["tile"])
-    s, upp = plan["splits"], plan["tiles_per_split"]
-    assert 1 <= s <= units and upp == -(-units // s)
-    assert plan["grid"] == nb * s < 2 ** 31
-    want = 16 * (s + jslots) * n if (s > 1 or jslots > 0) else 0
-    assert plan["scratch_bytes"] == want <= 24 << 30
+    spb = t // plan["tile"]
+    nd = _ndist(nb)
+    P, D, G = plan["splits"], plan["dists"], plan["groups"]
+    g, passes = plan["groups_per_pass"], plan["passes"]
+    assert 1 <= D <= nd and G == -(-nd // D)
+    assert 1 <= P <= max(1, D * spb) and plan["tiles_per_split"] == -(-min(D, nd) * spb // P)
+    assert 1 <= g <= G and passes == -(-G // g)
+    assert plan["grid"] == nb * P * g < 2 ** 31
+    rec = 16 * n
+    per_group = (P + _jslots(nb, D)) * rec
+    if nb == 1 and P == 1:
+        assert plan["scratch_bytes"] == plan["scratch_min_bytes"] == 0
+    elif passes == 1:
+        assert plan["scratch_bytes"] == G * per_group
+        assert plan["scratch_min_bytes"] == min(G * per_group, per_group + rec)
+    else:
+        assert plan["scratch_bytes"] == g * per_group + rec
+        assert plan["scratch_min_bytes"] == per_group + rec
     assert 0 < plan["fill"] <= 1.0
 
 
@@ -215,44 +308,85 @@ def test_symmetric_plan(lib, n, splits):
     plan = apg.nbody_plan_forces(n, 152, path=apg.NBODY_PATH_SYMMETRIC, splits=splits)
     assert plan["path"] == apg.NBODY_PATH_SYMMETRIC
     _sym_covers(plan, n)
+    assert plan["scratch_bytes"] <= max(apg.NBODY_DEFAULT_WORKSPACE_BYTES, 48 * n)
     if splits:
-        units = plan["tiles_per_split"] * plan["splits"]
-        assert plan["splits"] == min(splits, units) or plan["splits"] == splits
+        units = plan["dists"] * plan["threads"] * plan["i_per_thread"] // plan["tile"]
+        assert plan["splits"] == min(splits, max(1, units)) or plan["splits"] <= splits
 
 
 @pytest.mark.parametrize("sm", [1, 148, 160, 264])
 @pytest.mark.parametrize("n", [10240, 45056, 163840, 1048576, 2097159])
-@pytest.mark.parametrize("variant", [-1, 0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("variant", [-1, 0, 1, 2])
 def test_symmetric_plan_other_gpus_and_variants(n, sm, variant):
-    ref = apg.nbody_plan_forces(4096, 152, path=apg.NBODY_PATH_SYMMETRIC, variant=variant)
-    t = ref["threads"] * ref["i_per_thread"]
-    nb = -(-n // t)
-    jslots = (nb - 1) // 2 + (1 if nb % 2 == 0 else 0)
-    if variant >= 0 and 16 * (jslots + 1) * n > 24 << 30:   # partials beyond the cap
-        with pytest.raises(apg.NbodyError):
-            apg.nbody_plan_forces(n, sm, path=apg.NBODY_PATH_SYMMETRIC, variant=variant)
-        return
     plan = apg.nbody_plan_forces(n, sm, path=apg.NBODY_PATH_SYMMETRIC, variant=variant)
     assert plan["path"] == apg.NBODY_PATH_SYMMETRIC
     if variant >= 0:
         assert plan["variant"] == variant
     _sym_covers(plan, n)
+    assert plan["scratch_bytes"] <= apg.NBODY_DEFAULT_WORKSPACE_BYTES
 
 
-def test_symmetric_plan_forced_splits_stay_within_the_cap():
+def test_symmetric_plan_forced_splits_stay_within_the_budget():
     plan = apg.nbody_plan_forces(2 ** 21, 152, path=apg.NBODY_PATH_SYMMETRIC, splits=1000)
-    assert plan["scratch_bytes"] <= 24 << 30 and plan["splits"] < 1000
+    assert plan["scratch_bytes"] <= apg.NBODY_DEFAULT_WORKSPACE_BYTES and plan["splits"] < 1000
     _sym_covers(plan, 2 ** 21)
 
 
 def test_symmetric_plan_limits():
-    with pytest.raises(apg.NbodyError):      # j-side partials beyond 24 GiB
-        apg.nbody_plan_forces(2 ** 23, 152, path=apg.NBODY_PATH_SYMMETRIC)
     with pytest.raises(apg.NbodyError):      # the compensated kernel is tiled only
         apg.nbody_plan_forces(65536, 152, path=apg.NBODY_PATH_SYMMETRIC,
                               precision=apg.NBODY_PRECISION_COMPENSATED)
-    # automatic planning falls back to the tiled path where the partials do not fit
-    assert apg.nbody_plan_forces(2 ** 23, 152)["path"] == apg.NBODY_PATH_TILED
+    with pytest.raises(apg.NbodyError) as e:  # a forced symmetric path without room for a group
+        apg.nbody_plan_forces(65536, 152, path=apg.NBODY_PATH_SYMMETRIC, workspace_bytes=1 << 20)
+    assert e.value.status == 8
+    # the symmetric path serves every n: its workspace is bounded by a budget,
+    # not by n^2 (the pool-based calls allow one group's minimum beyond it)
+    for n in (2 ** 23, 2 ** 25, 2 ** 31 - 1):
+        plan = apg.nbody_plan_forces(n, 152)
+        assert plan["path"] == apg.NBODY_PATH_SYMMETRIC
+        _sym_covers(plan, n)
+        assert plan["scratch_bytes"] <= max(apg.NBODY_DEFAULT_WORKSPACE_BYTES, 48 * n)
+
+
+def test_default_workspace_at_one_million():
+    """The benchmark's call: the symmetric path within the default budget."""
+    plan = apg.nbody_plan_forces(1048576, 152)
+    assert plan["path"] == apg.NBODY_PATH_SYMMETRIC
+    assert 0 < plan["scratch_bytes"] <= apg.NBODY_DEFAULT_WORKSPACE_BYTES
+    assert plan["passes"] > 1 and plan["fill"] > 0.97
+
+
+@pytest.mark.parametrize("n", [20011, 65536, 200003, 1048576])
+def test_workspace_budget_changes_passes_not_the_decomposition(n):
+    """Every workspace of at least one group keeps the pieces, the distances
+    per group and therefore the partial sums and their order; only the
+    groups per pass change."""
+    base = apg.nbody_plan_forces(n, 152)
+    lo = base["scratch_min_bytes"]
+    seen_passes = set()
+    for budget in (lo, lo + 1, lo + 16 * n * 50, 2 * lo, 10 * lo, 1 << 40):
+        plan = apg.nbody_plan_forces(n, 152, workspace_bytes=budget)
+        assert (plan["path"], plan["variant"], plan["splits"], plan["dists"], plan["groups"]) == \
+               (base["path"], base["variant"], base["splits"], base["dists"], base["groups"])
+        assert plan["scratch_bytes"] <= budget
+        seen_passes.add(plan["passes"])
+        if budget == 1 << 40:
+            assert plan["passes"] == 1
+    # below one group the automatic choice runs without partials
+    none = apg.nbody_plan_forces(n, 152, workspace_bytes=0)
+    assert none["scratch_bytes"] == 0 and none["splits"] == 1
+
+
+def test_tiled_passes_within_a_workspace():
+    n = 200003
+    base = apg.nbody_plan_forces(n, 152, path=apg.NBODY_PATH_TILED)
+    assert base["splits"] > 2
+    for budget in (2 * 16 * n, 3 * 16 * n, 16 * n * base["splits"]):
+        plan = apg.nbody_plan_forces(n, 152, path=apg.NBODY_PATH_TILED, workspace_bytes=budget)
+        assert plan["splits"] == base["splits"] and plan["scratch_bytes"] <= budget
+        _covers(plan, n, budget)
+    small = apg.nbody_plan_forces(n, 152, path=apg.NBODY_PATH_TILED, workspace_bytes=16 * n)
+    assert small["splits"] == 1 and small["scratch_bytes"] == 0
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 31, 33, 127, 128, 129, 255, 257, 1000, 1024, 4096,
@@ -269,7 +403,8 @@ def test_plan_fills_the_gpu_at_one_million():
         assert plan["fill"] > 0.97
         one = apg.nbody_plan_forces(1048576, 152, path=path, splits=1)
         assert one["splits"] == 1
-        assert plan["fill"] > one["fill"]
+        if path == apg.NBODY_PATH_TILED:   # the symmetric path fills waves with groups too
+            assert plan["fill"] > one["fill"]
     one = apg.nbody_plan_forces(1048576, 152, path=apg.NBODY_PATH_TILED, splits=1)
     assert one["scratch_bytes"] == 0
 
@@ -298,6 +433,17 @@ def test_auto_path_choice():
         apg.nbody_plan_forces(1000, 152, path=apg.NBODY_PATH_CLUSTER, splits=3)
     with pytest.raises(apg.NbodyError):
         apg.nbody_plan_forces(1000, 152, path=7)
+    with pytest.raises(apg.NbodyError):      # distances per group belong to the symmetric path
+        apg.nbody_plan_forces(20000, 152, path=apg.NBODY_PATH_TILED, dists=3)
+    with pytest.raises(apg.NbodyError):
+        apg.nbody_plan_forces(20000, 152, quantities=2)
+
+
+def test_acceleration_only_plans_like_the_default():
+    for n in (1000, 8192, 20011, 1048576):
+        a = apg.nbody_plan_forces(n, 152)
+        b = apg.nbody_plan_forces(n, 152, quantities=apg.NBODY_QUANTITIES_ACC)
+        assert a == b
 
 
 def test_compensated_precision_plans_the_compensated_kernel():
@@ -335,3 +481,53 @@ def test_plan_forced_splits_and_variants(lib):
         apg.nbody_plan_forces(0, 152)
     with pytest.raises(apg.NbodyError):
         apg.nbody_plan_forces(1000, 0)
+    with pytest.raises(apg.NbodyError):
+        apg.nbody_plan_forces(1000, 152, workspace_bytes=-1)
+
+
+# ------------------------------------------------------------ workspace entry points
+
+SZ = ctypes.c_size_t
+
+
+def test_workspace_argument_checks(lib):
+    """The *_ws calls check the workspace like the body arrays (nothing below
+    reaches CUDA: each call is rejected on the host)."""
+    a, o = P, P + 4096
+    n = 10
+
+    def ws_call(ws, nbytes, pm=a, acc=o):
+        size = SZ(nbytes)
+        return lib.nbody_forces_ws(ctypes.c_void_p(pm), n, ctypes.c_float(1e-4),
+                                   ctypes.c_void_p(acc), None, ctypes.c_void_p(ws),
+                                   ctypes.byref(size), None)
+    assert ws_call(P + 8192 + 8, 1024) == 2            # misaligned workspace
+    assert ws_call(a + 64, 1024) == 3                  # workspace overlaps the bodies
+    assert ws_call(o - 512, 1024) == 3                 # workspace overlaps the output
+    assert ws_call(P + 8192, 1024, pm=a + 4) == 2      # body checks still apply
+    assert lib.nbody_forces_ws(ctypes.c_void_p(a), n, ctypes.c_float(1e-4), ctypes.c_void_p(o),
+                               None, ctypes.c_void_p(P + 8192), None, None) == 1   # no size
+    size = SZ(0)
+    assert lib.nbody_forces_ws(None, -1, ctypes.c_float(1e-4), None, None, None,
+                               ctypes.byref(size), None) == 1                    # bad n in a query
+    assert lib.nbody_forces_ws(None, 5, ctypes.c_float(0.0), None, None, None,
+                               ctypes.byref(size), None) == 1                    # bad eps2 in a query
+    assert lib.nbody_forces_ws(None, 0, ctypes.c_float(1e-4), None, None, None,
+                               ctypes.byref(size), None) == 0 and size.value == 0
+
+    def ts_call(ws, nbytes):
+        size = SZ(nbytes)
+        return lib.nbody_forces_ts_ws(ctypes.c_void_p(P), 5, ctypes.c_void_p(P + 4096), 7,
+                                      ctypes.c_float(1e-4), ctypes.c_void_p(P + 8192), None,
+                                      ctypes.c_void_p(ws), ctypes.byref(size), None)
+    assert ts_call(P + 4096 + 16, 64) == 3             # overlaps the sources
+    assert ts_call(P + 12288 + 4, 64) == 2
+
+    def sim_call(ws, nbytes):
+        size = SZ(nbytes)
+        return lib.nbody_simulate_ws(ctypes.c_void_p(a), ctypes.c_void_p(P + 4096),
+                                     ctypes.c_void_p(P + 8192), n, ctypes.c_float(1e-4),
+                                     ctypes.c_float(1e-3), 2, ctypes.c_void_p(ws),
+                                     ctypes.byref(size), None)
+    assert sim_call(P + 4096 + 32, 64) == 3            # overlaps the velocities
+    assert sim_call(P + 12288 + 8, 64) == 2

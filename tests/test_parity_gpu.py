@@ -73,6 +73,24 @@ def sample_rows(n, k, seed):
     return np.unique(np.concatenate([rows, [0, n - 1]]))
 
 
+def _hard_rows(w, k, seed, core=4096, block=2048):
+    """Rows where the per-body bound is most likely to fail, plus a random
+    sample: the `core` bodies nearest the centre of mass (densest region,
+    largest near-neighbour terms and cancellation), every body of the first,
+    a middle and the last `block`-body block (edges of the symmetric
+    decomposition), the ragged tail, and k random rows."""
+    n = w.n
+    x = w.pos_mass[:, :3].astype(np.float64)
+    m = w.pos_mass[:, 3].astype(np.float64)
+    com = (m[:, None] * x).sum(0) / m.sum()
+    r = np.linalg.norm(x - com, axis=1)
+    dense = np.argsort(r, kind="stable")[:min(core, n)]
+    mid = (n // block // 2) * block
+    edges = np.concatenate([np.arange(0, min(block, n)), np.arange(mid, min(mid + block, n)),
+                            np.arange(max(0, n - block), n)])
+    return np.unique(np.concatenate([sample_rows(n, k, seed), dense, edges]))
+
+
 # ------------------------------------------------------------ configurations
 
 def test_disk4096_acceleration_and_euler():
@@ -139,13 +157,13 @@ def test_plummer65536_trajectory_against_fp64():
     assert rx < 1e-6 and rv < 1e-5, (rx, rv)
 
 
-def test_clumps200003_sampled():
+def test_clumps200003_every_body():
+    """Every one of the 200003 bodies against the oracle (about 4e10 fp64
+    pairs on the host); the per-body maxima are printed."""
     w = W.named("clumps200003")
     acc = gpu_forces(w.pos_mass, w.eps2)
-    rows = sample_rows(w.n, 2048, 1)
-    # include the ragged last tile and the last i-block
-    rows = np.unique(np.concatenate([rows, np.arange(w.n - 300, w.n)]))
-    assert_parity(acc, oracle.forces(w.pos_mass, w.eps2, rows=rows), rows)
+    e = assert_parity(acc, oracle.forces(w.pos_mass, w.eps2))
+    print(f"clumps200003, all bodies: {e}")
 
 
 @pytest.mark.parametrize("name", ["clumps200003", "plummer65536"])
@@ -160,15 +178,20 @@ def test_tiled_path_at_large_n(name):
 
 
 @pytest.mark.slow
-def test_plummer1048576_sampled_in_bench_configuration():
+def test_plummer1048576_in_bench_configuration():
     """The full-size workload in the launch configuration the benchmark times
-    (default plan), checked on sampled rows."""
+    (default plan, several passes), checked on more than 16384 rows: the 4096
+    bodies of the dense core, every body of the first, a middle and the last
+    2048-body block, and 8192 random rows.  The per-body maxima are printed."""
     w = W.named("plummer1048576")
-    acc = gpu_forces(w.pos_mass, w.eps2)
-    rows = sample_rows(w.n, 768, 2)
-    assert_parity(acc, oracle.forces(w.pos_mass, w.eps2, rows=rows), rows)
     plan = apg.nbody_plan_forces(w.n, torch.cuda.get_device_properties(0).multi_processor_count)
-    assert plan["splits"] >= 1
+    assert plan["path"] == apg.NBODY_PATH_SYMMETRIC and plan["passes"] > 1
+    assert plan["scratch_bytes"] <= apg.NBODY_DEFAULT_WORKSPACE_BYTES
+    acc = gpu_forces(w.pos_mass, w.eps2)
+    rows = _hard_rows(w, 8192, seed=2)
+    assert rows.size >= 16384
+    e = assert_parity(acc, oracle.forces(w.pos_mass, w.eps2, rows=rows), rows)
+    print(f"plummer1048576, {rows.size} rows: {e}")
 
 
 @pytest.mark.parametrize("n", W.SMALL_SWEEP)
@@ -384,14 +407,27 @@ def test_symmetric_path_counts_every_pair_once(n, splits):
 
 @pytest.mark.slow
 def test_symmetric_path_partials_past_2_34_bytes():
-    """n = 2^21 + 7: 1025 blocks (odd) with a ragged last one, and 512 j-side
-    slots of n records: about 17 GB of partials, so their byte offsets pass
-    2^34; every body must have met every body exactly once."""
+    """n = 2^21 + 7: 1025 blocks (odd) with a ragged last one.  With a
+    caller's workspace large enough for every group in one pass, the partial
+    offsets pass 2^34 bytes; the result is bit-identical to the default call
+    (one group per pass, within the default budget), and every body met
+    every body exactly once."""
     n = 2 ** 21 + 7
-    plan = apg.nbody_plan_forces(n, torch.cuda.get_device_properties(0).multi_processor_count,
-                                 path=SYM)
-    assert plan["num_iblocks"] == 1025 and plan["scratch_bytes"] == 16 * (plan["splits"] + 512) * n
-    assert plan["scratch_bytes"] > 2 ** 34
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    base = apg.nbody_plan_forces(n, sm)
+    assert base["num_iblocks"] == 1025 and base["passes"] > 1
+    one = apg.nbody_plan_forces(n, sm, workspace_bytes=1 << 40)
+    assert one["passes"] == 1 and one["scratch_bytes"] > 2 ** 34
+    pm = np.zeros((n, 4), np.float32)
+    pm[:, :3] = W.Stream(n).uniform(3 * n, -1.0, 1.0).reshape(n, 3)
+    pm[:, 3] = 1.0
+    d_pm = torch.from_numpy(pm).to(dev())
+    ws = torch.empty(one["scratch_bytes"], dtype=torch.uint8, device=dev())
+    a = apg.nbody_forces_ws(d_pm, 2.0 ** 40, workspace=ws)
+    del ws
+    b = apg.nbody_forces(d_pm, 2.0 ** 40)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
     test_symmetric_path_counts_every_pair_once(n, 0)
 
 
@@ -627,6 +663,66 @@ def test_plummer1048576_properties_of_every_output():
         sel = (r >= lo) & (r < hi)
         model = -(1.0 / np.sqrt(1.0 + r[sel] ** 2) - 101.0 ** -1.5) / mtrunc
         assert abs(pself[sel].mean() / model.mean() - 1.0) < 0.01, (lo, hi)
+
+
+# ------------------------------------------------------------ acceleration only
+
+def gpu_forces_acc(pm_np, eps2, **kw):
+    pm = torch.from_numpy(np.ascontiguousarray(pm_np)).to(dev())
+    acc = apg.nbody_forces_ex(pm, float(eps2), quantities=apg.NBODY_QUANTITIES_ACC, **kw)
+    torch.cuda.synchronize()
+    return acc.cpu().numpy()
+
+
+def test_disk4096_acceleration_only():
+    """The disk workload checks the acceleration only: nbody_forces_acc
+    against the oracle over every body, its .w exactly 0."""
+    w = W.named("disk4096")
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    got = apg.nbody_forces_acc(pm, float(w.eps2))
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    assert np.all(got[:, 3] == 0.0)
+    assert_parity(got, oracle.forces(w.pos_mass, w.eps2), potential=False)
+
+
+@pytest.mark.parametrize("path", [1, 2, 3])
+@pytest.mark.parametrize("n", [1, 1000, 5003, 20011])
+def test_acceleration_only_every_path(path, n):
+    """Each kernel without its potential operations: the acceleration is the
+    same arithmetic, so it matches the a + p call bit for bit; .w is 0."""
+    w = W.clumps(n, seed=n + 5)
+    if path == 2 and n > 6144:
+        path = 1
+    full = gpu_forces(w.pos_mass, w.eps2, path=path)
+    acc = gpu_forces_acc(w.pos_mass, w.eps2, path=path)
+    assert np.array_equal(acc[:, :3], full[:, :3])
+    assert np.all(acc[:, 3] == 0.0)
+    assert_parity(acc, oracle.forces(w.pos_mass, w.eps2), potential=False)
+
+
+def test_acceleration_only_target_source_form():
+    t, s = _ts_bodies(3000, 20000, 77)
+    tt, ss = torch.from_numpy(t).to(dev()), torch.from_numpy(s).to(dev())
+    ws = torch.empty(0, device=dev())
+    out = apg.nbody_forces_ts_ws(tt, ss, 1e-3, workspace=ws, quantities=apg.NBODY_QUANTITIES_ACC)
+    full = apg.nbody_forces_ts(tt, ss, 1e-3)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out[:, 3]).item() == 0
+    # the same plan with the potential: identical accelerations
+    assert torch.equal(out[:, :3], apg.nbody_forces_ts_ws(tt, ss, 1e-3, workspace=ws)[:, :3])
+    assert_parity(out.cpu().numpy(), oracle.forces_ts(t, s, np.float32(1e-3)), potential=False)
+
+
+@pytest.mark.slow
+def test_plummer1048576_acceleration_only_sampled():
+    """The full-size workload without the potential, in the default plan:
+    sampled rows, the dense core included."""
+    w = W.named("plummer1048576")
+    acc = gpu_forces_acc(w.pos_mass, w.eps2)
+    rows = _hard_rows(w, 2048, seed=12)
+    assert_parity(acc, oracle.forces(w.pos_mass, w.eps2, rows=rows), rows, potential=False)
+    assert np.all(acc[:, 3] == 0.0)
 
 
 # ------------------------------------------------------------ concurrency
