@@ -2,7 +2,7 @@
 Plummer bodies (the headline workload), timed with CUDA events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config NAME] [--no-cpu-baseline] [--no-e2e] [--no-small-n]
+                    [--config NAME] [--no-cpu-baseline] [--no-e2e] [--no-configs]
 
 Prints one JSON line on rank 0.  `value` is interactions/s of the whole job
 (N^2 pairs per step and GPU) with inputs resident in HBM; `e2e` is the same
@@ -64,8 +64,10 @@ def parse():
                     help="force path of the timed step and e2e (auto: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-small-n", action="store_true",
-                    help="skip the small-N sweep (CUDA-graph-timed force calls, N = 1024..8192)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload table (every other configuration and the small-N "
+                         "sweep, CUDA-graph-timed), the acceleration-only call and the Euler "
+                         "HBM probe")
     ap.add_argument("--probe", choices=["euler", "configs"], default=None,
                     help="run one kernel probe alone and print its result (for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -86,35 +88,6 @@ def kernel_source_hash(kind):
         src = re.sub(r"//[^\n]*", " ", src)
         h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
-
-
-def small_n_sweep(apg, W, device, sizes=(1024, 2048, 4096, 8192), reps=20):
-    """Force-call time for the small-N sweep, replayed from a CUDA graph so that
-    host launch overhead is excluded; plus nbody_simulate's per-step time."""
-    import torch
-    out = []
-    for n in sizes:
-        w = W.small_cube(n)
-        pm = torch.from_numpy(w.pos_mass).to(device)
-        acc = torch.empty_like(pm)
-        eps2 = float(w.eps2)
-        best = graph_time_ms(lambda: apg.nbody_forces(pm, eps2, acc), reps)
-        vel = torch.zeros_like(pm)
-        steps = 100
-        apg.nbody_simulate(pm, vel, acc, eps2, float(w.dt), steps)
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        apg.nbody_simulate(pm, vel, acc, eps2, float(w.dt), steps)
-        b.record()
-        b.synchronize()
-        plan = apg.nbody_plan_forces(n, torch.cuda.get_device_properties(device).multi_processor_count)
-        out.append({"n": n, "forces_us": round(best * 1e3, 2),
-                    "interactions_per_s": float(n) * n / (best / 1e3),
-                    "simulate_us_per_step": round(a.elapsed_time(b) * 1e3 / steps, 2),
-                    "path": PATH_NAMES[plan["path"]],
-                    "cluster": plan["cluster"], "splits": plan["splits"]})
-    return out
 
 
 def euler_hbm_probe(apg, device, n=1 << 26, reps=5):
@@ -141,7 +114,7 @@ def euler_hbm_probe(apg, device, n=1 << 26, reps=5):
     return {"n": n, "ms": ms, "bytes": 80 * n, "gbs": 80 * n / (ms / 1e3) / 1e9}
 
 
-def force_roofline(plan, n, sm, sm_max_mhz):
+def force_roofline(plan, n, sm, sm_max_mhz, acc_only=False):
     """Arithmetic bound of the planned force kernel, in interactions/s.
 
     Ordered-pair kernels (tiled, cluster) execute 13 fp32 lane operations per
@@ -151,19 +124,21 @@ def force_roofline(plan, n, sm, sm_max_mhz):
     lane rate over the launch's lane operations, times its N^2 interactions."""
     lanes_per_s = sm * sm_max_mhz * 1e6 * FP32_LANES_PER_SM_CLK
     pairs = float(n) * float(n)
+    ordered = FP32_OPS_PER_PAIR - (1 if acc_only else 0)
+    unordered = SYM_OPS_PER_PAIR - (2 if acc_only else 0)
     if plan["path"] == PATH_SYMMETRIC:
         t = plan["threads"] * plan["i_per_thread"]
         nb = plan["num_iblocks"]
         last = n - (nb - 1) * t
         diag = float((nb - 1) * t * t + last * last)
-        ops = SYM_OPS_PER_PAIR / 2.0 * (pairs - diag) + FP32_OPS_PER_PAIR * diag
-        kind, kernel = "symmetric", "forces_sym_kernel (+ reduce_sym_kernel)"
+        ops = unordered / 2.0 * (pairs - diag) + ordered * diag
+        kind, kernel = "symmetric", "forces_sym_kernel (+ reduce_pass_kernel)"
     else:
-        ops = FP32_OPS_PER_PAIR * pairs
-        kind, kernel = "tiled", "forces_tiled_kernel (+ split reduction)"
+        ops = ordered * pairs
+        kind, kernel = "tiled", "forces_tiled_kernel (+ reduce_pass_kernel)"
     return {"peak": lanes_per_s * pairs / ops, "ops_per_interaction": ops / pairs,
             "kind": kind, "kernel": kernel,
-            "ordered_pair_peak": lanes_per_s / FP32_OPS_PER_PAIR}
+            "ordered_pair_peak": lanes_per_s / ordered}
 
 
 def measured_peaks():
@@ -366,7 +341,8 @@ def run_ours(args):
     pairs = float(n) * float(n)
     path = PATH_IDS[args.path]
     plan = apg.nbody_plan_forces(n, props.multi_processor_count, path=path)
-    launches_per_step = (2 if plan["scratch_bytes"] > 0 else 1) + 1
+    # force launches (with a reduction after each when partials are used), then Euler
+    launches_per_step = plan["passes"] * (2 if plan["scratch_bytes"] > 0 else 1) + 1
 
     pm0 = torch.from_numpy(w.pos_mass).to(device)
     vel0 = torch.from_numpy(w.vel).to(device)
@@ -426,9 +402,19 @@ def run_ours(args):
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = time_oracle(w, args.cpu_seconds)
+        # the whole evaluation on the host cores, extrapolated from the sample
+        cpu["extrapolated_full_n_seconds"] = float(n) * n / cpu["value"]
+        cpu["extrapolated_note"] = ("extrapolated: N^2 interactions at the sampled rate; "
+                                    "the full oracle evaluation is not run by the benchmark")
 
-    sweep = None if args.no_small_n else small_n_sweep(apg, W, device)
-    euler_hbm = None if args.no_small_n else euler_hbm_probe(apg, device)
+    configs = acc_only = euler_hbm = None
+    if not args.no_configs:
+        names = [c for c in W.CONFIG_NAMES if c != w.name] + [f"smallcube{k}" for k in W.SMALL_SWEEP]
+        cpu_on = not args.no_cpu_baseline and rank == 0 and world == 1
+        configs = configs_probe(apg, W, device, cpu_seconds=0.5 if cpu_on else 0,
+                                cpu1_seconds=0.3 if cpu_on else 0, names=names)
+        acc_only = acc_only_probe(apg, w, device, plan, props.multi_processor_count, sm_max)
+        euler_hbm = euler_hbm_probe(apg, device)
     src_hash = kernel_source_hash(roof["kind"])
     traffic = TRAFFIC_BY_SOURCE.get(src_hash) if w.name == "plummer1048576" else None
 
@@ -453,8 +439,9 @@ def run_ours(args):
                    "l2": "flushed (256 MiB write) before each timed step, outside its events",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "plan": {k: plan[k] for k in ("path", "variant", "i_per_thread", "threads",
-                                                 "tile", "num_iblocks", "splits", "grid",
-                                                 "scratch_bytes", "fill")}},
+                                                 "tile", "num_iblocks", "splits", "dists",
+                                                 "groups", "passes", "grid", "scratch_bytes",
+                                                 "fill")}},
         "roofline": {
             "bound": "alu",
             "achieved": achieved,
@@ -484,7 +471,8 @@ def run_ours(args):
                                      bound="hbm", peak_source=peaks_src)
                                 if euler_hbm else None)},
         "cpu_baseline": cpu,
-        "small_n": sweep,
+        "configs": configs,
+        "acc_only": acc_only,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
@@ -559,16 +547,20 @@ def graph_time_ms(fn, reps):
     return best
 
 
-def configs_probe(apg, W, device):
+def configs_probe(apg, W, device, cpu_seconds=1.5, cpu1_seconds=0.5, names=None):
     """Every measured workload: the force call alone (replayed from a CUDA
-    graph, so host launch overhead is excluded), one nbody_simulate step, and
-    the fraction of the fp32-pipe peak."""
+    graph, so host launch overhead is excluded), one nbody_simulate step, the
+    fraction of the planned kernel's fp32-pipe bound and of the ordered-pair
+    bound, and the oracle on a sample of rows (all host cores, and one core
+    for n <= 16384)."""
     import torch
     props = torch.cuda.get_device_properties(device)
     peaks, _ = measured_peaks()
     sm_max = float(peaks.get("sm_max_mhz", RECIPE_SM_MAX_MHZ))
     out = []
-    for name in W.CONFIG_NAMES + [f"smallcube{n}" for n in W.SMALL_SWEEP]:
+    if names is None:
+        names = W.CONFIG_NAMES + [f"smallcube{n}" for n in W.SMALL_SWEEP]
+    for name in names:
         w = W.named(name)
         n = w.n
         pm = torch.from_numpy(w.pos_mass).to(device)
@@ -589,18 +581,45 @@ def configs_probe(apg, W, device):
         plan = apg.nbody_plan_forces(n, props.multi_processor_count)
         roof = force_roofline(plan, n, props.multi_processor_count, sm_max)
         rate = float(n) * n / (ms / 1e3)
-        cpu = time_oracle(w, 1.5)
-        cpu1 = time_oracle(w, 0.5, threads=1) if n <= 16384 else None
+        cpu = time_oracle(w, cpu_seconds) if cpu_seconds > 0 else None
+        cpu1 = (time_oracle(w, cpu1_seconds, threads=1)
+                if cpu1_seconds > 0 and n <= 16384 else None)
         out.append({"workload": name, "n": n, "forces_ms": ms, "interactions_per_s": rate,
                     "gflops_20": rate * FLOPS_PER_PAIR / 1e9, "frac_fp32_peak": rate / roof["peak"],
                     "frac_of_ordered_pair_bound": rate / roof["ordered_pair_peak"],
                     "simulate_step_ms": step_ms,
                     "path": PATH_NAMES[plan["path"]],
-                    "splits": plan["splits"],
-                    "cpu_oracle_interactions_per_s": cpu["value"], "cpu_cores": cpu["cores"],
+                    "splits": plan["splits"], "passes": plan["passes"],
+                    "scratch_bytes": plan["scratch_bytes"],
+                    "cpu_oracle_interactions_per_s": cpu["value"] if cpu else None,
+                    "cpu_cores": cpu["cores"] if cpu else None,
                     "cpu_oracle_1thread_interactions_per_s": cpu1["value"] if cpu1 else None})
         del pm, vel, acc
     return out
+
+
+def acc_only_probe(apg, w, device, plan, sm, sm_max, reps=2):
+    """nbody_forces_acc on the headline workload: CUDA-event time of the
+    call, against the acceleration-only bound (16 fp32 lane operations per
+    unordered pair, 12 per ordered pair on the diagonal blocks)."""
+    import torch
+    pm = torch.from_numpy(w.pos_mass).to(device)
+    acc = torch.empty_like(pm)
+    apg.nbody_forces_acc(pm, float(w.eps2), acc)
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        apg.nbody_forces_acc(pm, float(w.eps2), acc)
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.mean(ts)
+    roof = force_roofline(plan, w.n, sm, sm_max, acc_only=True)
+    rate = float(w.n) * w.n / (ms / 1e3)
+    return {"call": "nbody_forces_acc", "forces_ms": ms, "interactions_per_s": rate,
+            "peak": roof["peak"], "frac": rate / roof["peak"],
+            "ops_per_interaction": roof["ops_per_interaction"], "runs": reps}
 
 
 def run_probe(args):
