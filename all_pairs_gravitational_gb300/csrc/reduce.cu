@@ -15,7 +15,9 @@
 //
 // HBM-bound: every slot record is read once (16 bytes), the carry read and
 // written once per pass.  A grid-stride loop over bodies, one thread per
-// body, keeps many independent loads in flight.
+// body; the slots a body reads in a group are consecutive records at stride
+// n (the i-side slots, then the j-side ones), read as runs with eight loads
+// in flight ahead of the dependent compensated adds.
 #include <algorithm>
 
 #include "nbody_device.cuh"
@@ -36,8 +38,24 @@ struct Kahan4 {
     }
 };
 
+// Add records p[0], p[n], ..., p[(cnt - 1) n] in that order.
+__device__ __forceinline__ void add_run(Kahan4 &k, const float4 *p, int64_t n, int cnt) {
+    constexpr int B = 8;
+    int s = 0;
+    for (; s + B <= cnt; s += B) {
+        float4 v[B];
+#pragma unroll
+        for (int u = 0; u < B; ++u) v[u] = __ldg(p + static_cast<int64_t>(s + u) * n);
+#pragma unroll
+        for (int u = 0; u < B; ++u) k.add(v[u]);
+    }
+    for (; s < cnt; ++s) k.add(__ldg(p + static_cast<int64_t>(s) * n));
+}
+
+constexpr int kReduceThreads = 128;
+
 template <bool SYM, bool EULER>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kReduceThreads)
 reduce_pass_kernel(const ReducePass rp, const EulerFuse eu) {
     const int64_t n = rp.n;
     const int H = (rp.nb - 1) / 2;
@@ -56,16 +74,21 @@ reduce_pass_kernel(const ReducePass rp, const EulerFuse eu) {
         // the extra distance nb / 2 of an even block count reaches only the
         // blocks nb / 2 .. nb - 1 (it is evaluated by the rows below nb / 2)
         const bool upper = SYM && even && (i / rp.block) >= rp.nb / 2;
-        for (int gl = 0; gl < rp.groups; ++gl) {
-            const float4 *base = rp.parts + static_cast<int64_t>(gl) * rp.gstride + i;
-            for (int s = 0; s < rp.islots; ++s) k.add(__ldg(base + static_cast<int64_t>(s) * n));
-            if (SYM) {
-                const int dlo = (rp.g0 + gl) * rp.D;
-                const int jbase = max(dlo, 1);
-                int dhi = min(dlo + rp.D, nd);
-                if (even && !upper) dhi = min(dhi, H + 1);
-                for (int d = jbase; d < dhi; ++d)
-                    k.add(__ldg(base + static_cast<int64_t>(rp.islots + d - jbase) * n));
+        if (!SYM && rp.gstride == static_cast<int64_t>(rp.islots) * n) {
+            // the tiled path: every group's slots follow one another
+            add_run(k, rp.parts + i, n, rp.groups * rp.islots);
+        } else {
+            for (int gl = 0; gl < rp.groups; ++gl) {
+                const float4 *base = rp.parts + static_cast<int64_t>(gl) * rp.gstride + i;
+                int cnt = rp.islots;
+                if (SYM) {   // j-side slots of distances jbase .. dhi - 1 follow the i-side ones
+                    const int dlo = (rp.g0 + gl) * rp.D;
+                    const int jbase = max(dlo, 1);
+                    int dhi = min(dlo + rp.D, nd);
+                    if (even && !upper) dhi = min(dhi, H + 1);
+                    cnt += max(0, dhi - jbase);
+                }
+                add_run(k, base, n, cnt);
             }
         }
         if (rp.final_pass) {
@@ -89,9 +112,10 @@ reduce_pass_kernel(const ReducePass rp, const EulerFuse eu) {
 template <bool SYM>
 cudaError_t launch_one(const ReducePass &rp, int grid, cudaStream_t stream, const EulerFuse *eu) {
     if (eu != nullptr)
-        reduce_pass_kernel<SYM, true><<<grid, 256, 0, stream>>>(rp, *eu);
+        reduce_pass_kernel<SYM, true><<<grid, kReduceThreads, 0, stream>>>(rp, *eu);
     else
-        reduce_pass_kernel<SYM, false><<<grid, 256, 0, stream>>>(rp, EulerFuse{nullptr, nullptr, 0.f});
+        reduce_pass_kernel<SYM, false><<<grid, kReduceThreads, 0, stream>>>(
+            rp, EulerFuse{nullptr, nullptr, 0.f});
     return cudaGetLastError();
 }
 
@@ -101,9 +125,8 @@ cudaError_t launch_reduce_pass(const ReducePass &rp, int sm_count, cudaStream_t 
                                const EulerFuse *euler) {
     if (rp.n <= 0 || rp.groups < 1 || rp.islots < 0) return cudaErrorInvalidValue;
     if (euler != nullptr && !rp.final_pass) return cudaErrorInvalidValue;
-    const int threads = 256;
-    const int64_t want = (static_cast<int64_t>(rp.n) + threads - 1) / threads;
-    const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sm_count) * 8));
+    const int64_t want = (static_cast<int64_t>(rp.n) + kReduceThreads - 1) / kReduceThreads;
+    const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sm_count) * 16));
     return rp.sym ? launch_one<true>(rp, grid, stream, euler)
                   : launch_one<false>(rp, grid, stream, euler);
 }
