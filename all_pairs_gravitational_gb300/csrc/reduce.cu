@@ -16,8 +16,8 @@
 // HBM-bound: every slot record is read once (16 bytes), the carry read and
 // written once per pass.  A grid-stride loop over bodies, one thread per
 // body; the slots a body reads in a group are consecutive records at stride
-// n (the i-side slots, then the j-side ones), read as runs with eight loads
-// in flight ahead of the dependent compensated adds.
+// n (the i-side slots, then the j-side ones), read as runs with up to sixteen
+// loads in flight ahead of the dependent compensated adds.
 #include <algorithm>
 
 #include "nbody_device.cuh"
@@ -38,9 +38,10 @@ struct Kahan4 {
     }
 };
 
-// Add records p[0], p[n], ..., p[(cnt - 1) n] in that order.
-__device__ __forceinline__ void add_run(Kahan4 &k, const float4 *p, int64_t n, int cnt) {
-    constexpr int B = 8;
+// Add records p[0], p[n], ..., p[(cnt - 1) n] in that order, B loads at a
+// time ahead of the adds.
+template <int B>
+__device__ __forceinline__ void add_run_b(Kahan4 &k, const float4 *p, int64_t n, int cnt) {
     int s = 0;
     for (; s + B <= cnt; s += B) {
         float4 v[B];
@@ -50,6 +51,13 @@ __device__ __forceinline__ void add_run(Kahan4 &k, const float4 *p, int64_t n, i
         for (int u = 0; u < B; ++u) k.add(v[u]);
     }
     for (; s < cnt; ++s) k.add(__ldg(p + static_cast<int64_t>(s) * n));
+}
+
+__device__ __forceinline__ void add_run(Kahan4 &k, const float4 *p, int64_t n, int cnt) {
+    if (cnt >= 16)
+        add_run_b<16>(k, p, n, cnt);
+    else
+        add_run_b<4>(k, p, n, cnt);
 }
 
 constexpr int kReduceThreads = 128;
