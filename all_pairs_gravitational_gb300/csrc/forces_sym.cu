@@ -303,6 +303,9 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
 //   3 CTAs per SM at K = 4 (12 % slower);
 //   each unit's cross-warp j-side sums spread over all threads, one component
 //   each, instead of one thread per source (1.2 % slower);
+//   the two halves of each j-side term shuffled back separately and added
+//   by the home lane as one packed add per step (halves added once per
+//   chunk): 6 % slower with the potential, equal without it;
 //   the potential terms or the j-side sums as scalar fp32 FMAs (6-10 %
 //   slower: packed f32x2 instructions occupy both halves of the FMA pipe, so
 //   no half is left idle for scalar work).
