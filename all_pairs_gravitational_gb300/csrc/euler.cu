@@ -22,6 +22,7 @@ namespace {
 __global__ void __launch_bounds__(256)
 euler_kernel(float4 *__restrict__ pm, float4 *__restrict__ vel,
              const float4 *__restrict__ acc, int n, float dt) {
+    pdl_wait_and_release();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += stride) {
@@ -40,8 +41,7 @@ cudaError_t launch_euler(float4 *pm, float4 *vel, const float4 *acc, int n, floa
     const int threads = 256;
     const int64_t want = (static_cast<int64_t>(n) + threads - 1) / threads;
     const int grid = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sm_count) * 8));
-    euler_kernel<<<grid, threads, 0, stream>>>(pm, vel, acc, n, dt);
-    return cudaGetLastError();
+    return launch_pdl(euler_kernel, dim3(grid), dim3(threads), 0, stream, 1, pm, vel, acc, n, dt);
 }
 
 }  // namespace nbody

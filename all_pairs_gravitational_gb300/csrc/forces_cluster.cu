@@ -206,6 +206,7 @@ forces_cluster_kernel(const Problem pr, int tiles_per_cta, int ntiles,
 
     __shared__ __align__(16) float sdup[kStages][P * 8];
     __shared__ __align__(16) float4 red[W][BI];
+    pdl_wait_and_release();
 
     const int warp = static_cast<int>(threadIdx.x) >> 5;
     const int lane = static_cast<int>(threadIdx.x) & 31;
@@ -258,6 +259,7 @@ forces_cluster_whole_kernel(const Problem pr, int tiles_per_cta, float4 *__restr
     constexpr int BI = 32 * K;
 
     extern __shared__ __align__(16) float4 dyn[];
+    pdl_wait_and_release();
     const int jc = tiles_per_cta * kClusterTile;          // sources staged by this CTA
     float *sdup = reinterpret_cast<float *>(dyn);          // jc bodies x 8 floats
     float4 (*red)[BI] = reinterpret_cast<float4 (*)[BI]>(dyn + 2 * jc);
@@ -293,55 +295,38 @@ forces_cluster_whole_kernel(const Problem pr, int tiles_per_cta, float4 *__restr
 template <int K, int W, int P>
 cudaError_t launch_tiled_cluster(const Problem &pr, int num_ib, int cluster, int tpc, int ntiles,
                                  float4 *out, cudaStream_t stream, const EulerFuse *eu) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(num_ib) * static_cast<unsigned>(cluster), 1, 1);
-    cfg.blockDim = dim3(W * 32, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const dim3 grid(static_cast<unsigned>(num_ib) * static_cast<unsigned>(cluster));
+    const dim3 block(W * 32);
+    const unsigned cx = static_cast<unsigned>(cluster);
     const EulerFuse none = {nullptr, nullptr, 0.f};
     if (eu != nullptr)
-        return pr.pot ? cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true, true>, pr,
-                                           tpc, ntiles, out, *eu)
-                      : cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, false, true>, pr,
-                                           tpc, ntiles, out, *eu);
-    return pr.pot ? cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, true, false>, pr, tpc,
-                                       ntiles, out, none)
-                  : cudaLaunchKernelEx(&cfg, forces_cluster_kernel<K, W, P, false, false>, pr, tpc,
-                                       ntiles, out, none);
+        return pr.pot ? launch_pdl(forces_cluster_kernel<K, W, P, true, true>, grid, block, 0,
+                                   stream, cx, pr, tpc, ntiles, out, *eu)
+                      : launch_pdl(forces_cluster_kernel<K, W, P, false, true>, grid, block, 0,
+                                   stream, cx, pr, tpc, ntiles, out, *eu);
+    return pr.pot ? launch_pdl(forces_cluster_kernel<K, W, P, true, false>, grid, block, 0, stream,
+                               cx, pr, tpc, ntiles, out, none)
+                  : launch_pdl(forces_cluster_kernel<K, W, P, false, false>, grid, block, 0, stream,
+                               cx, pr, tpc, ntiles, out, none);
 }
 
 template <int K, int W>
 cudaError_t launch_whole(const Problem &pr, int num_ib, int cluster, int tpc, float4 *out,
                          cudaStream_t stream, const EulerFuse *eu) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(num_ib) * static_cast<unsigned>(cluster), 1, 1);
-    cfg.blockDim = dim3(W * 32, 1, 1);
-    cfg.dynamicSmemBytes = whole_smem_bytes(K, W, tpc);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const dim3 grid(static_cast<unsigned>(num_ib) * static_cast<unsigned>(cluster));
+    const dim3 block(W * 32);
+    const size_t smem = whole_smem_bytes(K, W, tpc);
+    const unsigned cx = static_cast<unsigned>(cluster);
     const EulerFuse none = {nullptr, nullptr, 0.f};
     if (eu != nullptr)
-        return pr.pot ? cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, true, true>, pr,
-                                           tpc, out, *eu)
-                      : cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, false, true>, pr,
-                                           tpc, out, *eu);
-    return pr.pot ? cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, true, false>, pr, tpc,
-                                       out, none)
-                  : cudaLaunchKernelEx(&cfg, forces_cluster_whole_kernel<K, W, false, false>, pr,
-                                       tpc, out, none);
+        return pr.pot ? launch_pdl(forces_cluster_whole_kernel<K, W, true, true>, grid, block,
+                                   smem, stream, cx, pr, tpc, out, *eu)
+                      : launch_pdl(forces_cluster_whole_kernel<K, W, false, true>, grid, block,
+                                   smem, stream, cx, pr, tpc, out, *eu);
+    return pr.pot ? launch_pdl(forces_cluster_whole_kernel<K, W, true, false>, grid, block, smem,
+                               stream, cx, pr, tpc, out, none)
+                  : launch_pdl(forces_cluster_whole_kernel<K, W, false, false>, grid, block, smem,
+                               stream, cx, pr, tpc, out, none);
 }
 
 #define NBODY_CLUSTER(K, W, P)                                                             \

@@ -152,6 +152,7 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
 
     extern __shared__ __align__(16) unsigned char smem[];
     float4 (*jacc)[W][SUB] = reinterpret_cast<float4 (*)[W][SUB]>(smem);
+    pdl_wait_and_release();
 
     const int tid = static_cast<int>(threadIdx.x);
     const int lane = tid & 31;
@@ -328,13 +329,12 @@ cudaError_t launch_sym_variant(const float *bodies, int n, float eps2, bool pot,
                           static_cast<unsigned>(sl.groups);
     const float4 *b4 = reinterpret_cast<const float4 *>(bodies);
     constexpr size_t smem = SymShape<K, W, SUB>::smem_bytes;
-    if (pot)
-        forces_sym_kernel<K, W, SUB, MINB, U, GF, true><<<grid, W * 32, smem, stream>>>(
-            b4, n, eps2, sl.nb, sl.P, sl.D, sl.g0, parts, sl.gstride);
-    else
-        forces_sym_kernel<K, W, SUB, MINB, U, GF, false><<<grid, W * 32, smem, stream>>>(
-            b4, n, eps2, sl.nb, sl.P, sl.D, sl.g0, parts, sl.gstride);
-    return cudaGetLastError();
+    return pot ? launch_pdl(forces_sym_kernel<K, W, SUB, MINB, U, GF, true>, dim3(grid),
+                            dim3(W * 32), smem, stream, 1, b4, n, eps2, sl.nb, sl.P, sl.D, sl.g0,
+                            parts, sl.gstride)
+               : launch_pdl(forces_sym_kernel<K, W, SUB, MINB, U, GF, false>, dim3(grid),
+                            dim3(W * 32), smem, stream, 1, b4, n, eps2, sl.nb, sl.P, sl.D, sl.g0,
+                            parts, sl.gstride);
 }
 
 typedef cudaError_t (*SymLauncher)(const float *, int, float, bool, const SymLaunch &, float4 *,

@@ -65,6 +65,7 @@ forces_tiled_kernel(const Problem pr, int num_ib, int piece0, int tiles_per_spli
 
     __shared__ __align__(16) float sdup[kStages][P * 8];
     __shared__ __align__(16) f2 stot[TSMEM ? KP * 8 : 1][TSMEM ? NT : 1];
+    pdl_wait_and_release();
 
     const int tid = static_cast<int>(threadIdx.x);
     const int ib = static_cast<int>(blockIdx.x % static_cast<unsigned>(num_ib));
@@ -216,13 +217,10 @@ template <int K, int NT, int P, int MINB, bool TS, int U, int MODE>
 cudaError_t launch_variant(const Problem &pr, int num_ib, int piece0, int pieces, int tps,
                            int ntiles, float4 *out, cudaStream_t stream) {
     const unsigned grid = static_cast<unsigned>(num_ib) * static_cast<unsigned>(pieces);
-    if (pr.pot)
-        forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, true><<<grid, NT, 0, stream>>>(
-            pr, num_ib, piece0, tps, ntiles, out);
-    else
-        forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, false><<<grid, NT, 0, stream>>>(
-            pr, num_ib, piece0, tps, ntiles, out);
-    return cudaGetLastError();
+    return pr.pot ? launch_pdl(forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, true>, dim3(grid),
+                               dim3(NT), 0, stream, 1, pr, num_ib, piece0, tps, ntiles, out)
+                  : launch_pdl(forces_tiled_kernel<K, NT, P, MINB, TS, U, MODE, false>, dim3(grid),
+                               dim3(NT), 0, stream, 1, pr, num_ib, piece0, tps, ntiles, out);
 }
 
 typedef cudaError_t (*TiledLauncher)(const Problem &, int, int, int, int, int, float4 *,

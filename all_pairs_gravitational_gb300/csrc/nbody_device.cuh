@@ -91,6 +91,19 @@ __device__ __forceinline__ void euler_body(float4 &x, float4 &v, const float4 &a
     v.z = __fadd_rn(v.z, __fmul_rn(dt, a.z));
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization allowed, so the hardware may start
+// scheduling its CTAs while the previous kernel in the stream is finishing.
+// Each kernel first waits for the previous grid to complete with its memory
+// visible -- before touching any global memory, so the ordering is the same
+// as plain stream order -- and only then lets the next grid be scheduled
+// (so at most one grid waits ahead of a running one).  Only the launch and
+// CTA scheduling latency overlap.
+__device__ __forceinline__ void pdl_wait_and_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

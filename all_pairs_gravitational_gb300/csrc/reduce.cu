@@ -65,6 +65,7 @@ constexpr int kReduceThreads = 128;
 template <bool SYM, bool EULER>
 __global__ void __launch_bounds__(kReduceThreads)
 reduce_pass_kernel(const ReducePass rp, const EulerFuse eu) {
+    pdl_wait_and_release();
     const int64_t n = rp.n;
     const int H = (rp.nb - 1) / 2;
     const bool even = rp.nb % 2 == 0;
@@ -120,11 +121,10 @@ reduce_pass_kernel(const ReducePass rp, const EulerFuse eu) {
 template <bool SYM>
 cudaError_t launch_one(const ReducePass &rp, int grid, cudaStream_t stream, const EulerFuse *eu) {
     if (eu != nullptr)
-        reduce_pass_kernel<SYM, true><<<grid, kReduceThreads, 0, stream>>>(rp, *eu);
-    else
-        reduce_pass_kernel<SYM, false><<<grid, kReduceThreads, 0, stream>>>(
-            rp, EulerFuse{nullptr, nullptr, 0.f});
-    return cudaGetLastError();
+        return launch_pdl(reduce_pass_kernel<SYM, true>, dim3(grid), dim3(kReduceThreads), 0,
+                          stream, 1, rp, *eu);
+    return launch_pdl(reduce_pass_kernel<SYM, false>, dim3(grid), dim3(kReduceThreads), 0, stream,
+                      1, rp, EulerFuse{nullptr, nullptr, 0.f});
 }
 
 }  // namespace
