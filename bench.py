@@ -38,9 +38,10 @@ PATH_SYMMETRIC = 3
 PATH_NAMES = {1: "tiled", 2: "cluster", 3: "symmetric"}
 PATH_IDS = {"auto": 0, "tiled": 1, "symmetric": 3}
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
-# the force kernel at N = 2^20, from one ncu capture, keyed by a hash of the
-# kernel's source files: a changed kernel reports null until it is re-measured.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the force
+# kernel's launches in one force call at N = 2^20, from one ncu capture, keyed
+# by a hash of the kernel's source files: a changed kernel reports null until
+# it is re-measured.
 KERNEL_SOURCES = {
     "tiled": ["all_pairs_gravitational_gb300/csrc/forces_tiled.cu",
               "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"],
@@ -48,7 +49,8 @@ KERNEL_SOURCES = {
                   "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"],
 }
 TRAFFIC_BY_SOURCE = {
-    "4859a3519e6993b0": {"bytes": 419.08e6 + 4.56e9,
+    # one nbody_forces call = 7 passes of the symmetric kernel (default plan)
+    "38e6a797d7d47b0e": {"bytes": 495.2e6 + 5738.4e6,
                          "profile": "profiles/forces_sym_plummer1048576_dram.md"},
 }
 
