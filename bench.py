@@ -66,7 +66,7 @@ def parse():
                     help="force path of the timed step and e2e (auto: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-configs", action="store_true",
+    ap.add_argument("--no-configs", "--no-small-n", dest="no_configs", action="store_true",
                     help="skip the per-workload table (every other configuration and the small-N "
                          "sweep, CUDA-graph-timed), the acceleration-only call and the Euler "
                          "HBM probe")
