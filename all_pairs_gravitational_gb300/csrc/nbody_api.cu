@@ -199,7 +199,6 @@ nbody_status device_pool(DeviceState *d, cudaMemPool_t *pool) {
 // decomposition without partials.
 
 constexpr int kDefaultTiledVariant = 0;
-constexpr int kDefaultClusterVariant = 0;
 constexpr int kCompensatedTiledVariant = 7;
 constexpr int kMaxSplits = 1024;
 constexpr int64_t kDesignBudget = NBODY_DEFAULT_WORKSPACE_BYTES;
@@ -365,10 +364,27 @@ void plan_cluster_variant(int64_t nt, int64_t ns, int sm, int occ, int variant, 
     *t_out = best_t;
 }
 
-// Largest n the automatic choice sends to the cluster path (measured on
-// GB300 inside CUDA graphs: the cluster path is ahead up to 4096 bodies, the
-// tiled one from 8192).
-constexpr int64_t kClusterMaxN = 6144;
+// Largest n the automatic choice sends to the cluster path, and the cluster
+// variant it takes by size.  Measured on GB300 inside CUDA graphs (force
+// call, microseconds) over variants 0 (K = 2, 4 warps, 128-body tiles), 6
+// (K = 2, 8 warps, whole range staged), 7 (K = 4, 8 warps, whole range) and
+// the tiled path; the times jump with the integer counts of target blocks,
+// cluster sizes and waves, so the choice is a table of the measured best:
+//   n:        2560  3072  3584  4096  4352  4608  4864  5120  5376  5632  5888  6144
+//   v0:       8.29  8.49 12.77 12.86 15.39 15.47 26.66 25.97 31.60 31.58 31.46 31.96
+//   v6:       9.62 12.85 16.08 13.95 15.42 15.46 28.98 19.67 22.73 22.72 26.34 34.46
+//   v7:       9.85  9.80 12.06 12.06 14.44 16.98 20.48 25.53 27.92 27.91 30.10 30.17
+//   tiled:   13.07 13.27 13.68 13.86 22.98 22.98 23.25 23.02 23.55 23.57 23.96 24.23
+// (1024-2048 bodies: variant 0 fastest, 3.5-5.3 us.)
+constexpr int64_t kClusterMaxN = 5632;
+
+int auto_cluster_variant(int64_t n) {
+    if (n <= 3072) return 0;
+    if (n <= 4352) return 7;
+    if (n <= 4608) return 0;
+    if (n <= 4864) return 7;
+    return 6;
+}
 
 // Symmetric path (each unordered pair once).  Smallest n the automatic choice
 // sends to it, and the variant it takes by size, measured on GB300 inside
@@ -577,10 +593,9 @@ nbody_status make_plan_uncached(int64_t nt, int64_t ns, bool all_pairs, int sm,
     if (o.splits != 0) return NBODY_ERR_INVALID_ARG;   // the cluster path plans its own split
     if (o.variant >= nbody::cluster_variant_count()) return NBODY_ERR_INVALID_ARG;
     // The cost model picks the cluster size well but ranks the kernel
-    // variants poorly; measured inside CUDA graphs on GB300, variant 0 is the
-    // fastest or within a few percent from 1024 to 6144 bodies, so automatic
-    // planning uses it and a forced variant is honoured.
-    const int only = o.variant >= 0 ? o.variant : kDefaultClusterVariant;
+    // variants poorly, so automatic planning takes the variant from the
+    // measured table above; a forced variant is honoured.
+    const int only = o.variant >= 0 ? o.variant : auto_cluster_variant(std::max(nt, ns));
     double t = INFINITY;
     plan_cluster_variant(nt, ns, sm, occ.cluster[only], only, p, &t);
     // a forced whole-range variant whose range cannot fit shared memory
