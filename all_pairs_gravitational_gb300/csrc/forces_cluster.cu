@@ -23,13 +23,20 @@
 // buffer, so that a small-N time step is one launch instead of two.
 //
 // Reduction, deterministic and without atomics or global scratch:
-//   1. each warp folds its fp32 partials into Kahan totals and writes them to
-//      shared memory;
-//   2. the CTA adds its W warp partials in the order w = 0 .. W-1;
-//   3. after a cluster barrier, CTA c adds slice c of the targets over the C
-//      CTAs' shared memory, rank 0 .. C-1, and stores the result;
-//   4. a second cluster barrier keeps every CTA's shared memory alive until
-//      the other CTAs have read it.
+//   0. every thread arrives at a cluster barrier when the kernel starts;
+//   1. after the pair loop each warp folds its fp32 partials into Kahan
+//      totals and writes them to shared memory, and the CTA adds its W warp
+//      partials in the order w = 0 .. W-1;
+//   2. after waiting on the start barrier (every CTA of the cluster has
+//      started, so its shared memory exists), the CTA stores each target's
+//      partial straight into the inbox of the CTA that owns that target
+//      (CTA c owns slice c of the target block), in the sender's slot;
+//   3. a second cluster barrier (release / acquire) makes the stores
+//      visible, and each owner adds its inbox in rank order 0 .. C-1,
+//      compensated, and stores the result.
+//   No CTA touches another's shared memory after step 3's barrier, so none
+//   has to wait for the others before exiting (one cluster barrier fewer
+//   than reading the partials from the other CTAs).
 #include <algorithm>
 
 #include "nbody_device.cuh"
@@ -37,10 +44,10 @@
 
 namespace nbody {
 
-// Dynamic shared memory of the whole-range kernel: the staged range and the
-// per-warp partials.
+// Dynamic shared memory of the whole-range kernel: the staged range, the
+// per-warp partials and the inbox of the cluster reduction.
 size_t whole_smem_bytes(int K, int W, int tiles_per_cta) {
-    return static_cast<size_t>(tiles_per_cta) * 128 * 32 + static_cast<size_t>(W) * 32 * K * 16;
+    return static_cast<size_t>(tiles_per_cta) * 128 * 32 + static_cast<size_t>(W + 1) * 32 * K * 16;
 }
 
 namespace {
@@ -61,20 +68,26 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
     return r;
 }
 
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Load a float4 from the shared memory of CTA `rank` of this cluster, at the
-// offset `local` has in this CTA's shared memory.
-__device__ __forceinline__ float4 ld_dsmem_f4(const void *local, uint32_t rank) {
+// Store a float4 into the shared memory of CTA `rank` of this cluster, at
+// the offset `local` has in this CTA's shared memory.
+__device__ __forceinline__ void st_dsmem_f4(void *local, uint32_t rank, float4 v) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(remote), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
 }
 
 __device__ __forceinline__ void kahan4(float4 &h, float4 &c, const float4 &v) {
@@ -131,10 +144,12 @@ struct WarpAcc {
     }
 };
 
-// Steps 1-4 of the reduction: warp partials -> CTA partial -> cluster sum ->
-// out[ib * BI + slot] for this CTA's slice of the target block.
+// Steps 1-3 of the reduction: warp partials -> CTA partial -> the owner
+// CTAs' inboxes -> out[ib * BI + slot] for this CTA's slice of the target
+// block.  `red` holds W * 32 K records (warp partials), `box` 32 K (the
+// inbox: [sender rank][slot within a slice]).
 template <int K, int W, bool POT, bool EULER>
-__device__ __forceinline__ void reduce_and_store(WarpAcc<K / 2> &acc, float4 (*red)[32 * K],
+__device__ __forceinline__ void reduce_and_store(WarpAcc<K / 2> &acc, float4 *red, float4 *box,
                                                  int ib, const Problem &pr,
                                                  float4 *__restrict__ out, const EulerFuse &eu) {
     constexpr int KP = K / 2;
@@ -143,7 +158,10 @@ __device__ __forceinline__ void reduce_and_store(WarpAcc<K / 2> &acc, float4 (*r
     const int tid = static_cast<int>(threadIdx.x);
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    // 1. warp partials to shared memory: slot k*32 + lane is target ib*BI + slot
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t csize = cluster_nctarank();
+    const int per = BI / static_cast<int>(csize);
+    // 1. warp partials to shared memory: slot k * 32 + lane is target ib * BI + slot
 #pragma unroll
     for (int q = 0; q < KP; ++q) {
         float x0, x1, y0, y1, z0, z1, p0 = 0.f, p1 = 0.f;
@@ -151,29 +169,29 @@ __device__ __forceinline__ void reduce_and_store(WarpAcc<K / 2> &acc, float4 (*r
         f2_unpack(f2_sub(acc.hy[q], acc.ly[q]), y0, y1);
         f2_unpack(f2_sub(acc.hz[q], acc.lz[q]), z0, z1);
         if (POT) f2_unpack(f2_sub(acc.hp[q], acc.lp[q]), p0, p1);
-        red[warp][(2 * q) * 32 + lane] = make_float4(x0, y0, z0, p0);
-        red[warp][(2 * q + 1) * 32 + lane] = make_float4(x1, y1, z1, p1);
+        red[warp * BI + (2 * q) * 32 + lane] = make_float4(x0, y0, z0, p0);
+        red[warp * BI + (2 * q + 1) * 32 + lane] = make_float4(x1, y1, z1, p1);
     }
     __syncthreads();
-    // 2. CTA partial over warps w = 0 .. W-1, in place in red[0]
+    // 2. the CTA partial over warps 0 .. W-1, stored into the owner's inbox
+    cluster_wait();   // every CTA of the cluster has started
     for (int slot = tid; slot < BI; slot += NT) {
-        float4 h = red[0][slot];
+        float4 h = red[slot];
         float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 1; w < W; ++w) kahan4(h, c, red[w][slot]);
-        red[0][slot] = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y),
-                                   __fsub_rn(h.z, c.z), __fsub_rn(h.w, c.w));
+        for (int w = 1; w < W; ++w) kahan4(h, c, red[w * BI + slot]);
+        st_dsmem_f4(&box[static_cast<int>(crank) * per + slot % per],
+                    static_cast<uint32_t>(slot / per),
+                    make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y), __fsub_rn(h.z, c.z),
+                                __fsub_rn(h.w, c.w)));
     }
-    // 3. cluster partial over ranks 0 .. C-1 for this CTA's slice of targets
+    // 3. every store of the cluster is visible: this CTA's slice, rank order
     cluster_sync();
-    const uint32_t crank = cluster_ctarank();
-    const uint32_t csize = cluster_nctarank();
-    const int per = BI / static_cast<int>(csize);
     for (int t = tid; t < per; t += NT) {
-        const int slot = static_cast<int>(crank) * per + t;
         float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 c = h;
-        for (uint32_t r = 0; r < csize; ++r) kahan4(h, c, ld_dsmem_f4(&red[0][slot], r));
+        for (uint32_t r = 0; r < csize; ++r) kahan4(h, c, box[static_cast<int>(r) * per + t]);
+        const int slot = static_cast<int>(crank) * per + t;
         const int64_t i = static_cast<int64_t>(ib) * BI + slot;
         if (i < pr.nt) {
             const float4 a = make_float4(__fsub_rn(h.x, c.x), __fsub_rn(h.y, c.y),
@@ -188,8 +206,6 @@ __device__ __forceinline__ void reduce_and_store(WarpAcc<K / 2> &acc, float4 (*r
             }
         }
     }
-    // 4. keep this CTA's shared memory alive until every rank has read it
-    cluster_sync();
 }
 
 template <int K, int W, int P, bool POT, bool EULER>
@@ -205,8 +221,10 @@ forces_cluster_kernel(const Problem pr, int tiles_per_cta, int ntiles,
     static_assert(P % W == 0 && JW <= kFoldJ, "tile must split evenly, <= 32 sources per warp");
 
     __shared__ __align__(16) float sdup[kStages][P * 8];
-    __shared__ __align__(16) float4 red[W][BI];
+    __shared__ __align__(16) float4 red[W * BI];
+    __shared__ __align__(16) float4 box[BI];
     pdl_wait_and_release();
+    cluster_arrive_relaxed();   // matched by the wait before the partials are pushed
 
     const int warp = static_cast<int>(threadIdx.x) >> 5;
     const int lane = static_cast<int>(threadIdx.x) & 31;
@@ -243,7 +261,7 @@ forces_cluster_kernel(const Problem pr, int tiles_per_cta, int ntiles,
         stage = (stage + 1 == kStages) ? 0 : stage + 1;
     }
     cp_async_wait<0>();
-    reduce_and_store<K, W, POT, EULER>(acc, red, ib, pr, out, eu);
+    reduce_and_store<K, W, POT, EULER>(acc, red, box, ib, pr, out, eu);
 }
 
 // Whole-range variant: see the file header.  The CTA's range is
@@ -260,9 +278,11 @@ forces_cluster_whole_kernel(const Problem pr, int tiles_per_cta, float4 *__restr
 
     extern __shared__ __align__(16) float4 dyn[];
     pdl_wait_and_release();
+    cluster_arrive_relaxed();   // matched by the wait before the partials are pushed
     const int jc = tiles_per_cta * kClusterTile;          // sources staged by this CTA
     float *sdup = reinterpret_cast<float *>(dyn);          // jc bodies x 8 floats
-    float4 (*red)[BI] = reinterpret_cast<float4 (*)[BI]>(dyn + 2 * jc);
+    float4 *red = dyn + 2 * jc;
+    float4 *box = red + W * BI;
 
     const int warp = static_cast<int>(threadIdx.x) >> 5;
     const int lane = static_cast<int>(threadIdx.x) & 31;
@@ -289,7 +309,7 @@ forces_cluster_whole_kernel(const Problem pr, int tiles_per_cta, float4 *__restr
         acc.fold_acc();
         if (POT) acc.fold_pot();
     }
-    reduce_and_store<K, W, POT, EULER>(acc, red, ib, pr, out, eu);
+    reduce_and_store<K, W, POT, EULER>(acc, red, box, ib, pr, out, eu);
 }
 
 template <int K, int W, int P>

@@ -366,24 +366,24 @@ void plan_cluster_variant(int64_t nt, int64_t ns, int sm, int occ, int variant, 
 
 // Largest n the automatic choice sends to the cluster path, and the cluster
 // variant it takes by size.  Measured on GB300 inside CUDA graphs (force
-// call, microseconds) over variants 0 (K = 2, 4 warps, 128-body tiles), 6
-// (K = 2, 8 warps, whole range staged), 7 (K = 4, 8 warps, whole range) and
-// the tiled path; the times jump with the integer counts of target blocks,
-// cluster sizes and waves, so the choice is a table of the measured best:
-//   n:        2560  3072  3584  4096  4352  4608  4864  5120  5376  5632  5888  6144
-//   v0:       8.29  8.49 12.77 12.86 15.39 15.47 26.66 25.97 31.60 31.58 31.46 31.96
-//   v6:       9.62 12.85 16.08 13.95 15.42 15.46 28.98 19.67 22.73 22.72 26.34 34.46
-//   v7:       9.85  9.80 12.06 12.06 14.44 16.98 20.48 25.53 27.92 27.91 30.10 30.17
-//   tiled:   13.07 13.27 13.68 13.86 22.98 22.98 23.25 23.02 23.55 23.57 23.96 24.23
-// (1024-2048 bodies: variant 0 fastest, 3.5-5.3 us.)
-constexpr int64_t kClusterMaxN = 5632;
+// call, microseconds, two sweeps agreeing within 0.1 us) over variants 0
+// (K = 2, 4 warps, 128-body tiles), 6 (K = 2, 8 warps, whole range staged),
+// 7 (K = 4, 8 warps, whole range) and the tiled path; the times jump with the
+// integer counts of target blocks, cluster sizes and waves, so the choice is
+// a table of the measured best:
+//   n:      2048  2560  3072  3584  4096  4352  4608  4864  5120  5376  5632  6144
+//   v0:     4.81  8.20  8.33 12.66 12.74 15.26 15.25 26.52 25.64 31.27 31.02 31.63
+//   v6:     5.01  8.98 10.40 12.80 12.97 14.36 14.36 27.56 27.61 30.27 30.28 25.71
+//   v7:     6.87  9.47  9.48 11.67 11.66 14.05 16.53 20.04 25.29 27.64 27.72 29.91
+//   tiled: 12.53 12.93 13.26 13.62 13.92 22.73 22.94 23.13 23.38 23.78 23.49 24.31
+// (1024 bodies: variant 0, 3.2 us.)
+constexpr int64_t kClusterMaxN = 4864;
 
 int auto_cluster_variant(int64_t n) {
     if (n <= 3072) return 0;
     if (n <= 4352) return 7;
-    if (n <= 4608) return 0;
-    if (n <= 4864) return 7;
-    return 6;
+    if (n <= 4608) return 6;
+    return 7;
 }
 
 // Symmetric path (each unordered pair once).  Smallest n the automatic choice

@@ -692,7 +692,7 @@ def test_acceleration_only_every_path(path, n):
     """Each kernel without its potential operations: the acceleration is the
     same arithmetic, so it matches the a + p call bit for bit; .w is 0."""
     w = W.clumps(n, seed=n + 5)
-    if path == 2 and n > 5632:
+    if path == 2 and n > 4864:
         path = 1
     full = gpu_forces(w.pos_mass, w.eps2, path=path)
     acc = gpu_forces_acc(w.pos_mass, w.eps2, path=path)

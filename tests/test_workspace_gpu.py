@@ -124,8 +124,8 @@ def test_no_workspace_runs_without_partials(n):
     pm = torch.from_numpy(w.pos_mass).to(dev())
     out = apg.nbody_forces_ws(pm, float(w.eps2), workspace=torch.empty(0, device=dev()))
     torch.cuda.synchronize()
-    ref = apg.nbody_forces_ex(pm, float(w.eps2), path=apg.NBODY_PATH_TILED if n > 5632 else 0,
-                              splits=1 if n > 5632 else 0)
+    ref = apg.nbody_forces_ex(pm, float(w.eps2), path=apg.NBODY_PATH_TILED if n > 4864 else 0,
+                              splits=1 if n > 4864 else 0)
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
     rows = rows_of(n, 1000, 6)
