@@ -544,6 +544,23 @@ bool plan_sym(int64_t n, int sm, int occ, int variant, int splits_req, int dists
     return true;
 }
 
+// Tiled variant for all-pairs calls below the symmetric path, measured on
+// GB300 inside CUDA graphs (force call, microseconds): variant 0 (K = 4, 256
+// threads: 1024-target blocks) against variant 6 (K = 2, 256 threads,
+// two sources per step: 512-target blocks),
+//   n:     5120  6144  7168  8192  9216 10239 12288
+//   v0:    23.2  24.2  38.0  38.6  53.8  55.2  70.3
+//   v6:    19.9  25.2  31.9  40.5  44.7  58.4  74.5
+// The smaller blocks win when the count of 1024-target blocks is odd (the
+// pieces then fill the waves worse), so that is the rule.
+constexpr int kSmallTiledVariant = 6;
+
+int auto_tiled_variant(int64_t nt, int64_t ns, bool all_pairs) {
+    if (all_pairs && nt == ns && nt < kSymMinN && (ceil_div(nt, 1024) & 1))
+        return kSmallTiledVariant;
+    return kDefaultTiledVariant;
+}
+
 int auto_sym_variant(int64_t n) {
     return n < kSymMidN ? kSymSmallVariant : (n < kSymLargeN ? kSymMidVariant : kDefaultSymVariant);
 }
@@ -584,7 +601,7 @@ nbody_status make_plan_uncached(int64_t nt, int64_t ns, bool all_pairs, int sm,
                    : NBODY_ERR_WORKSPACE;
     }
     if (path == NBODY_PATH_TILED) {
-        const int variant = o.variant < 0 ? kDefaultTiledVariant : o.variant;
+        const int variant = o.variant < 0 ? auto_tiled_variant(nt, ns, all_pairs) : o.variant;
         if (variant >= nbody::tiled_variant_count() || variant >= kMaxVariants)
             return NBODY_ERR_INVALID_ARG;
         plan_tiled(nt, ns, sm, occ.tiled[variant], variant, o.splits, budget, p);
