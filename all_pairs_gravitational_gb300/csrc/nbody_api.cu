@@ -817,6 +817,10 @@ nbody_status default_workspace(int64_t nt, int64_t ns, bool all_pairs,
 // the key changes, the old graph is destroyed and its pool memory freed in
 // stream order behind its last replay.
 
+// Steps per batch graph, and the largest n that gets one.
+constexpr int kSimBatch = 16;
+constexpr int64_t kSimBatchMaxN = 65536;
+
 struct SimKey {
     const float *pm;
     float *vel;
@@ -839,6 +843,7 @@ struct SimGraph {
     SimKey key = {};
     cudaGraphExec_t exec = nullptr;    // one step: forces (+ reduction), then Euler
     cudaGraphExec_t exec2 = nullptr;   // small N: two steps with Euler fused into the forces
+    cudaGraphExec_t execb = nullptr;   // up to 65536 bodies: kSimBatch steps in one graph
     void *pool_mem = nullptr;          // pool memory of the workspace (nullptr: the caller's)
     cudaEvent_t done = nullptr;        // recorded after the latest replay
 };
@@ -849,7 +854,7 @@ cudaStream_t g_capture[kMaxDevices] = {};
 
 nbody_status sim_release(SimGraph &g, cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
-    for (cudaGraphExec_t *x : {&g.exec, &g.exec2}) {
+    for (cudaGraphExec_t *x : {&g.exec, &g.exec2, &g.execb}) {
         if (*x != nullptr) {
             const cudaError_t ex = cudaGraphExecDestroy(*x);
             if (e == cudaSuccess) e = ex;
@@ -971,14 +976,49 @@ nbody_status sim_build(int dev_id, DeviceState *dev, const SimKey &k, SimGraph &
             return el;
         }, &exec2);
     }
+    // Up to 65536 bodies a step is short enough that launching one graph per
+    // step (or pair) shows: kSimBatch steps are captured into one graph,
+    // where each kernel's launch overlaps the previous one's tail.
+    cudaGraphExec_t execb = nullptr;
+    if (e == cudaSuccess && k.n <= kSimBatchMaxN) {
+        if (exec2 != nullptr) {
+            float4 *pb = reinterpret_cast<float4 *>(static_cast<char *>(ws) + plan.scratch_bytes);
+            const nbody::Problem pr_b = {reinterpret_cast<const float *>(pb),
+                                         reinterpret_cast<const float *>(pb), ni, ni, k.eps2, true};
+            const int ntiles = static_cast<int>(ceil_div(k.n, plan.tile));
+            const nbody::EulerFuse to_b = {pb, vel, k.dt};
+            const nbody::EulerFuse to_a = {pos, vel, k.dt};
+            e = capture_graph(cap, [&](cudaStream_t s) {
+                cudaError_t el = cudaSuccess;
+                for (int t = 0; t < kSimBatch / 2 && el == cudaSuccess; ++t) {
+                    el = nbody::launch_cluster(plan.variant, pr, plan.num_iblocks, plan.cluster,
+                                               plan.tiles_per_split, ntiles, acc, s, &to_b);
+                    if (el == cudaSuccess)
+                        el = nbody::launch_cluster(plan.variant, pr_b, plan.num_iblocks,
+                                                   plan.cluster, plan.tiles_per_split, ntiles, acc,
+                                                   s, &to_a);
+                }
+                return el;
+            }, &execb);
+        } else {
+            e = capture_graph(cap, [&](cudaStream_t s) {
+                cudaError_t el = cudaSuccess;
+                for (int t = 0; t < kSimBatch && el == cudaSuccess; ++t)
+                    el = launch_step(plan, pr, acc, parts, dev->sm_count, pos, vel, k.dt, s);
+                return el;
+            }, &execb);
+        }
+    }
     if (e != cudaSuccess) {
         if (exec != nullptr) cudaGraphExecDestroy(exec);
+        if (exec2 != nullptr) cudaGraphExecDestroy(exec2);
         if (pool_mem != nullptr) cudaFreeAsync(pool_mem, stream);
         return cuda_fail(e);
     }
     g.key = k;
     g.exec = exec;
     g.exec2 = exec2;
+    g.execb = execb;
     g.pool_mem = pool_mem;
     g.valid = true;
     return NBODY_OK;
@@ -1012,6 +1052,9 @@ nbody_status run_simulate(float *pos_mass, float *vel, float *acc_pot, int64_t n
     cudaError_t e = cudaStreamWaitEvent(stream, g.done, 0);   // after the previous replay
     if (e != cudaSuccess) return cuda_fail(e);
     int64_t left = steps;
+    if (g.execb != nullptr)
+        for (; left >= kSimBatch; left -= kSimBatch)
+            if ((e = cudaGraphLaunch(g.execb, stream)) != cudaSuccess) return cuda_fail(e);
     if (g.exec2 != nullptr)
         for (; left >= 2; left -= 2)
             if ((e = cudaGraphLaunch(g.exec2, stream)) != cudaSuccess) return cuda_fail(e);

@@ -529,11 +529,14 @@ def _separate_steps(w, steps):
 
 
 @pytest.mark.parametrize("name,steps", [("smallcube1024", 20), ("smallcube1024", 7),
-                                        ("smallcube4096", 3), ("smallcube8192", 4),
-                                        ("plummer65536", 10), ("clumps200003", 2)])
+                                        ("smallcube1024", 37), ("smallcube4096", 3),
+                                        ("smallcube8192", 4), ("smallcube8192", 33),
+                                        ("cube16384", 17), ("plummer65536", 10),
+                                        ("clumps200003", 2)])
 def test_simulate_is_the_separate_calls(name, steps):
     """Cluster path (fused pairs of steps), tiled path (8192) and symmetric
-    path (65536, 200003)."""
+    path (16384, 65536, 200003); 37, 33 and 17 steps run through the
+    16-step batch graph and then the pair and single-step graphs."""
     w = W.named(name)
     ref = _separate_steps(w, steps)
     pm = torch.from_numpy(w.pos_mass).to(dev())
