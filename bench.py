@@ -427,7 +427,7 @@ def run_ours(args):
                                     "the full oracle evaluation is not run by the benchmark")
 
     configs = acc_only = euler_hbm = None
-    if not args.no_configs:
+    if not args.no_configs and world == 1:   # single-GPU figures; a scaling run skips them
         names = [c for c in W.CONFIG_NAMES if c != w.name] + [f"smallcube{k}" for k in W.SMALL_SWEEP]
         cpu_on = not args.no_cpu_baseline and rank == 0 and world == 1
         configs = configs_probe(apg, W, device, cpu_seconds=0.5 if cpu_on else 0,
