@@ -259,3 +259,50 @@ def test_pool_shortage_falls_back_to_a_plan_without_partials():
     assert torch.equal(out, no_partials)
     rows = rows_of(n, 800, 9)
     assert_parity(out.cpu().numpy(), oracle.forces(w.pos_mass, w.eps2, rows=rows), rows)
+
+
+# ------------------------------------------------------------ randomized shapes
+
+def _random_cases(count=24, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for k in range(count):
+        n = int(rng.integers(1, 30000))
+        path = int(rng.choice([0, 1, 2, 3]))
+        if path == 2 and n > 12000:
+            path = 0
+        dists = int(rng.choice([0, 1, 2, 5])) if path == 3 else 0
+        splits = int(rng.choice([0, 1, 3, 17])) if path in (1, 3) else 0
+        cases.append((k, n, path, dists, splits))
+    return cases
+
+
+@pytest.mark.parametrize("k,n,path,dists,splits", _random_cases())
+def test_random_shapes_budgets_and_paths(k, n, path, dists, splits):
+    """Seeded random sizes, paths, distances per group and pieces: the
+    result within a workspace of the least size that keeps the plan, and
+    within the default, agree bit for bit and match the oracle."""
+    w = W.clumps(n, seed=k + 7) if k % 2 else W.cube(n, seed=k + 7)
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    kw = dict(path=path, dists=dists, splits=splits)
+    plan = apg.nbody_plan_forces(n, sm_count(), **kw)
+    ref = apg.nbody_forces_ex(pm, float(w.eps2), **kw)
+    lo = max(plan["scratch_min_bytes"], 16)
+    out = apg.nbody_forces_ws(pm, float(w.eps2), workspace=workspace(lo), **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref), plan
+    rows = rows_of(n, 300, k)
+    assert_parity(ref.cpu().numpy(), oracle.forces(w.pos_mass, w.eps2, rows=rows), rows)
+
+
+def test_target_source_workspace_on_one_array_is_the_symmetric_call():
+    """nbody_forces_ts_ws with the same array as targets and sources takes
+    the symmetric path within the caller's workspace: the bits of
+    nbody_forces."""
+    w = W.clumps(30011, seed=31)
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    ref = apg.nbody_forces(pm, float(w.eps2))
+    ws = workspace(apg.nbody_forces_workspace_bytes(w.n))
+    out = apg.nbody_forces_ts_ws(pm, pm, float(w.eps2), workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
