@@ -28,6 +28,12 @@
  *     launches nothing and leaves every buffer untouched.  No kernel traps,
  *     asserts or spins on a flag.
  *   - n is an int64_t; n == 0 is a successful no-op; 0 < n <= 2^31 - 1.
+ *   - Every kernel is launched with programmatic stream serialization and
+ *     lets the next kernel of its stream be scheduled once it has started;
+ *     it waits for the previous kernel to complete before touching memory.
+ *     A caller's own kernel launched with that attribute after a library
+ *     call must wait likewise (cudaGridDependencySynchronize) before reading
+ *     the results.
  *
  * Device memory.  Large problems add partial sums in a second kernel; the
  * partials need a workspace.  Two ways to provide it:
@@ -165,8 +171,11 @@ nbody_status nbody_forces_ts(const float *targets, int64_t nt, const float *sour
  *                   step's starting positions.
  *   steps         : >= 0 (0 is a no-op).
  *
- * One step is captured once into a CUDA graph and replayed `steps` times on
- * `stream`.  The library keeps one such graph per device, keyed by the
+ * One step is captured once into a CUDA graph and replayed on `stream`; up
+ * to 65536 bodies a second graph holds 16 steps (and on the small-n path a
+ * third holds two with the Euler update fused into the force kernel), and
+ * `steps` runs as batches of 16, then pairs, then single steps.  The
+ * library keeps one set of graphs per device, keyed by the
  * pointers, n, eps2, dt and the workspace; a call with other arguments
  * rebuilds it (tens of microseconds).  The graph's workspace (the partials,
  * and at small n a second position buffer) comes from the library's pool and
