@@ -6,22 +6,23 @@ The compute path lives in ``libnbody.so`` (hand-written sm_103a CUDA, see
 use.
 """
 from ._binding import (EXPORTS, LIB_PATH, NBODY_DEFAULT_WORKSPACE_BYTES, NBODY_NOALLOC_MAX_N,
-                       NBODY_PATH_AUTO, NBODY_PATH_CLUSTER, NBODY_PATH_SYMMETRIC,
+                       NBODY_PATH_AUTO, NBODY_PATH_CLUSTER, NBODY_PATH_ROWS, NBODY_PATH_SYMMETRIC,
                        NBODY_PATH_TILED, NBODY_POOL_KEEP_BYTES, NBODY_PRECISION_COMPENSATED,
                        NBODY_PRECISION_DEFAULT, NBODY_QUANTITIES_ACC, NBODY_QUANTITIES_ACC_POT,
                        NbodyError, load_library, nbody_euler_step, nbody_forces, nbody_forces_acc,
                        nbody_forces_ex, nbody_forces_noalloc, nbody_forces_ts,
                        nbody_forces_ts_ws, nbody_forces_workspace_bytes, nbody_forces_ws,
-                       nbody_last_cuda_error, nbody_plan_forces, nbody_release_cached,
+                       nbody_last_cuda_error, nbody_plan_forces, nbody_plan_forces_ts,
+                       nbody_release_cached,
                        nbody_simulate, nbody_simulate_workspace_bytes, nbody_simulate_ws,
                        nbody_status_string)
 
 __all__ = ["EXPORTS", "LIB_PATH", "NBODY_DEFAULT_WORKSPACE_BYTES", "NBODY_NOALLOC_MAX_N",
-           "NBODY_PATH_AUTO", "NBODY_PATH_CLUSTER", "NBODY_PATH_SYMMETRIC", "NBODY_PATH_TILED",
+           "NBODY_PATH_AUTO", "NBODY_PATH_CLUSTER", "NBODY_PATH_ROWS", "NBODY_PATH_SYMMETRIC", "NBODY_PATH_TILED",
            "NBODY_POOL_KEEP_BYTES", "NBODY_PRECISION_COMPENSATED", "NBODY_PRECISION_DEFAULT",
            "NBODY_QUANTITIES_ACC", "NBODY_QUANTITIES_ACC_POT", "NbodyError", "load_library",
            "nbody_euler_step", "nbody_forces", "nbody_forces_acc", "nbody_forces_ex",
            "nbody_forces_noalloc", "nbody_forces_ts", "nbody_forces_ts_ws",
-           "nbody_forces_workspace_bytes", "nbody_forces_ws", "nbody_last_cuda_error",
+           "nbody_forces_workspace_bytes", "nbody_forces_ws", "nbody_last_cuda_error", "nbody_plan_forces_ts",
            "nbody_plan_forces", "nbody_release_cached", "nbody_simulate",
            "nbody_simulate_workspace_bytes", "nbody_simulate_ws", "nbody_status_string"]

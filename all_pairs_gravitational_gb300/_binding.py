@@ -18,6 +18,7 @@ NBODY_PATH_AUTO = 0
 NBODY_PATH_TILED = 1
 NBODY_PATH_CLUSTER = 2
 NBODY_PATH_SYMMETRIC = 3
+NBODY_PATH_ROWS = 4
 NBODY_PRECISION_DEFAULT = 0
 NBODY_PRECISION_COMPENSATED = 1
 NBODY_QUANTITIES_ACC_POT = 0
@@ -36,7 +37,7 @@ NBODY_NOALLOC_MAX_N = 4194304
 # Every symbol include/nbody.h declares (checked by the tests).
 EXPORTS = ["nbody_forces", "nbody_forces_acc", "nbody_euler_step", "nbody_status_string",
            "nbody_last_cuda_error", "nbody_release_cached", "nbody_plan_forces",
-           "nbody_plan_forces_ws", "nbody_forces_ex", "nbody_forces_ws", "nbody_forces_ts_ws",
+           "nbody_plan_forces_ws", "nbody_plan_forces_ts", "nbody_forces_ex", "nbody_forces_ws", "nbody_forces_ts_ws",
            "nbody_simulate_ws", "nbody_forces_noalloc", "nbody_forces_ts", "nbody_simulate"]
 
 
@@ -91,6 +92,8 @@ _SIGS = {
     "nbody_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "nbody_last_cuda_error": ([], ctypes.c_int),
     "nbody_plan_forces": ([ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P], ctypes.c_int),
+    "nbody_plan_forces_ts": ([ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P,
+                              ctypes.c_int64, _P], ctypes.c_int),
     "nbody_forces_noalloc": ([_P, ctypes.c_int64, ctypes.c_float, _P, _P], ctypes.c_int),
     "nbody_forces_ts": ([_P, ctypes.c_int64, _P, ctypes.c_int64, ctypes.c_float, _P, _P],
                         ctypes.c_int),
@@ -427,4 +430,20 @@ def nbody_plan_forces(n, sm_count, ctas_per_sm=0, path=NBODY_PATH_AUTO, variant=
                                       int(workspace_bytes), ctypes.byref(plan))
     if st != 0:
         raise NbodyError(st, "nbody_plan_forces")
+    return plan.as_dict()
+
+
+def nbody_plan_forces_ts(nt, ns, sm_count, ctas_per_sm=0, path=NBODY_PATH_AUTO, variant=-1,
+                         splits=0, quantities=NBODY_QUANTITIES_ACC_POT, workspace_bytes=None):
+    """Host-only: the decomposition nbody_forces_ts would launch for nt targets
+    and ns sources in separate arrays (a dict)."""
+    lib = load_library()
+    plan = nbody_plan()
+    opts = _opts(path, variant, splits, NBODY_PRECISION_DEFAULT, quantities, 0)
+    st = lib.nbody_plan_forces_ts(int(nt), int(ns), int(sm_count), int(ctas_per_sm),
+                                  ctypes.byref(opts),
+                                  -1 if workspace_bytes is None else int(workspace_bytes),
+                                  ctypes.byref(plan))
+    if st != 0:
+        raise NbodyError(st, "nbody_plan_forces_ts")
     return plan.as_dict()

@@ -154,6 +154,13 @@ nbody_status device_state(DeviceState **out) {
                                                               sv.warps * 32, sv.smem);
             if (e != cudaSuccess) return cuda_fail(e);
         }
+        for (int v = 0; v < nbody::rows_variant_count(); ++v) {
+            const nbody::RowsVariant &rv = nbody::rows_variant(v);
+            for (const void *fn : {rv.fn_pot, rv.fn_acc, rv.fn_pot_euler, rv.fn_acc_euler})
+                if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(nbody::kRowsSmemMax))) != cudaSuccess)
+                    return cuda_fail(e);
+        }
         d.ready = true;
     }
     *out = &d;
@@ -364,26 +371,141 @@ void plan_cluster_variant(int64_t nt, int64_t ns, int sm, int occ, int variant, 
     *t_out = best_t;
 }
 
-// Largest n the automatic choice sends to the cluster path, and the cluster
-// variant it takes by size.  Measured on GB300 inside CUDA graphs (force
-// call, microseconds, two sweeps agreeing within 0.1 us) over variants 0
-// (K = 2, 4 warps, 128-body tiles), 6 (K = 2, 8 warps, whole range staged),
-// 7 (K = 4, 8 warps, whole range) and the tiled path; the times jump with the
-// integer counts of target blocks, cluster sizes and waves, so the choice is
-// a table of the measured best:
+// The cluster variant a forced cluster-path call takes by size (the
+// automatic choice sends small calls to the row-split path instead).
+// Measured on GB300 inside CUDA graphs (force call, microseconds) over
+// variants 0 (K = 2, 4 warps, 128-body tiles), 6 (K = 2, 8 warps, whole
+// range staged) and 7 (K = 4, 8 warps, whole range); the times jump with
+// the integer counts of target blocks, cluster sizes and waves, so the
+// choice is a table of the measured best:
 //   n:      2048  2560  3072  3584  4096  4352  4608  4864  5120  5376  5632  6144
 //   v0:     4.81  8.20  8.33 12.66 12.74 15.26 15.25 26.52 25.64 31.27 31.02 31.63
 //   v6:     5.01  8.98 10.40 12.80 12.97 14.36 14.36 27.56 27.61 30.27 30.28 25.71
 //   v7:     6.87  9.47  9.48 11.67 11.66 14.05 16.53 20.04 25.29 27.64 27.72 29.91
-//   tiled: 12.53 12.93 13.26 13.62 13.92 22.73 22.94 23.13 23.38 23.78 23.49 24.31
 // (1024 bodies: variant 0, 3.2 us.)
-constexpr int64_t kClusterMaxN = 4864;
-
 int auto_cluster_variant(int64_t n) {
     if (n <= 3072) return 0;
     if (n <= 4352) return 7;
     if (n <= 4608) return 6;
     return 7;
+}
+
+// Row-split path (few sources): CTA b takes targets [b tb, (b + 1) tb) with
+// tb = ceil(nt / SMs), so every SM gets the same share of the pairs; its
+// warp items are K targets against one of S pieces of the sources, a piece
+// holding at most kRowsPieceMax sources.  Cost model, in units of one
+// target's 32-column step at the FMA pipe's rate: item `it` runs on warp
+// it mod W, whose scheduler is it mod 4 (W is a multiple of 4), so the
+// busiest scheduler runs ceil(items / 4) items of K x (steps + the row
+// sums' shuffle tree, about kRowsTreeSteps steps) each; and a warp runs
+// ceil(items / W) items one after another, each step at least one
+// dependency chain long (kRowsStepLatency units), which sets the time when
+// few items share a scheduler.  S is the cheapest count by that model, the
+// fewest on a tie.
+constexpr int64_t kRowsPieceMax = 2048;
+// The automatic choice takes the row-split path when both the targets and
+// the sources number fewer than this (from 10240 all-pairs bodies the
+// symmetric path is as fast: 50.7 against 50.5 us at 10240, 69.7 against
+// 70.6 us at 12288).  Against the tiled and cluster paths, measured inside
+// CUDA graphs on GB300 (force call, us):
+//   n:         1024  2048  3072  4096  4864  6144  8192
+//   row-split: 2.54  3.99  6.80  9.35 13.29 19.36 31.42
+//   before:    3.19  4.85  8.28 11.66 20.08 24.17 38.65   (cluster to 4864, then tiled)
+constexpr int64_t kRowsMaxAutoN = 10240;
+constexpr double kRowsTreeSteps = 2.5;
+constexpr double kRowsStepLatency = 2.3;
+constexpr int64_t kRowsMaxPieces = 64;
+
+bool plan_rows(int64_t nt, int64_t ns, int sm, int variant, int forced_pieces, nbody_plan *p,
+               double *t_out = nullptr) {
+    const nbody::RowsVariant &v = nbody::rows_variant(variant);
+    const int64_t K = v.i_per_warp;
+    const int64_t tb = ceil_div(nt, sm);
+    const int64_t grid = ceil_div(nt, tb);
+    const int64_t groups = ceil_div(tb, K);
+    const int64_t s_lo = forced_pieces > 0 ? forced_pieces
+                                           : std::max<int64_t>(1, ceil_div(ns, kRowsPieceMax));
+    const int64_t s_hi = forced_pieces > 0 ? forced_pieces : std::max(s_lo, kRowsMaxPieces);
+    double best_t = INFINITY;
+    int64_t best_s = 0, best_cols = 0;
+    for (int64_t s = s_lo; s <= s_hi; ++s) {
+        const int64_t cols = ceil_div(ns, 64 * s) * 32;
+        const int64_t ns_pad = 2 * s * cols;
+        if (ns_pad > INT32_MAX || groups * K * s > INT32_MAX ||
+            nbody::rows_smem_bytes(static_cast<int>(ns_pad), static_cast<int>(s),
+                                   static_cast<int>(groups * K)) > nbody::kRowsSmemMax)
+            continue;
+        const double steps = static_cast<double>(cols / 32);
+        const double t =
+            static_cast<double>(ceil_div(groups * s, 4)) * static_cast<double>(K) *
+                (steps + kRowsTreeSteps) +
+            static_cast<double>(ceil_div(groups * s, v.warps)) * steps * kRowsStepLatency;
+        if (t < best_t * (1.0 - 1e-9)) {
+            best_t = t;
+            best_s = s;
+            best_cols = cols;
+        }
+    }
+    if (best_s == 0) return false;   // the sources (or the piece sums) exceed shared memory
+    if (t_out != nullptr) *t_out = best_t;
+    const int64_t items = groups * best_s;
+    p->path = NBODY_PATH_ROWS;
+    p->variant = variant;
+    p->i_per_thread = static_cast<int32_t>(K);
+    p->threads = v.warps * 32;
+    p->tile = static_cast<int32_t>(2 * best_cols);
+    p->num_iblocks = static_cast<int32_t>(grid);
+    p->splits = static_cast<int32_t>(best_s);
+    p->tiles_per_split = static_cast<int32_t>(tb);
+    p->cluster = 1;
+    p->warps_j = v.warps;
+    p->dists = 0;
+    p->groups = 1;
+    p->groups_per_pass = 1;
+    p->passes = 1;
+    p->grid = grid;
+    p->scratch_bytes = 0;
+    p->scratch_min_bytes = 0;
+    // useful pairs over the pair slots of the busiest schedulers
+    p->fill = static_cast<double>(nt) * static_cast<double>(ns) /
+              (static_cast<double>(sm) * 4.0 * static_cast<double>(ceil_div(items, 4)) *
+               static_cast<double>(K) * static_cast<double>(2 * best_cols));
+    return true;
+}
+
+// The automatic row-split plan: the variant (K targets per item: 7, 6, or 4
+// with 12 warps) with the cheapest modelled time, the first on a tie.
+// Measured on GB300 inside CUDA graphs (force call, us), the model picks
+// the fastest of the three at every size measured:
+//   n:       1024  2048  3072  4096  4864  6144  8192 10239
+//   K = 7:   2.59  4.11  6.98  9.51 14.46 19.60 32.42 51.37
+//   K = 6:   2.95  5.26  7.24 11.58 15.12 21.36 33.92 54.38
+//   K = 4:   2.79  4.92  7.11 10.91 12.99 20.77 33.41 51.42
+bool plan_rows_auto(int64_t nt, int64_t ns, int sm, int forced_pieces, nbody_plan *p) {
+    double best_t = INFINITY;
+    bool found = false;
+    for (int v : {0, 1, 2}) {
+        nbody_plan q = {};
+        double t = INFINITY;
+        if (plan_rows(nt, ns, sm, v, forced_pieces, &q, &t) && t < best_t * (1.0 - 1e-9)) {
+            best_t = t;
+            *p = q;
+            found = true;
+        }
+    }
+    return found;
+}
+
+// The kernel-side decomposition of a row-split plan.
+nbody::RowsLaunch rows_launch(const nbody_plan &plan) {
+    nbody::RowsLaunch rl;
+    rl.tb = plan.tiles_per_split;
+    rl.groups = (plan.tiles_per_split + plan.i_per_thread - 1) / plan.i_per_thread;
+    rl.tb_pad = rl.groups * plan.i_per_thread;
+    rl.pieces = plan.splits;
+    rl.cols = plan.tile / 2;
+    rl.ns_pad = plan.splits * plan.tile;
+    return rl;
 }
 
 // Symmetric path (each unordered pair once).  Smallest n the automatic choice
@@ -571,6 +693,7 @@ nbody_status make_plan_uncached(int64_t nt, int64_t ns, bool all_pairs, int sm,
     nbody_forces_opts o = o_in;
     if (o.precision == NBODY_PRECISION_COMPENSATED) {   // the tiled path's compensated kernel
         if (o.path == NBODY_PATH_CLUSTER || o.path == NBODY_PATH_SYMMETRIC ||
+            o.path == NBODY_PATH_ROWS ||
             (o.variant >= 0 && o.variant != kCompensatedTiledVariant))
             return NBODY_ERR_INVALID_ARG;
         o.path = NBODY_PATH_TILED;
@@ -582,8 +705,8 @@ nbody_status make_plan_uncached(int64_t nt, int64_t ns, bool all_pairs, int sm,
         return NBODY_ERR_INVALID_ARG;
     int path = o.path;
     if (path == NBODY_PATH_AUTO) {
-        if (nt <= kClusterMaxN && ns <= kClusterMaxN) {
-            path = NBODY_PATH_CLUSTER;
+        if (nt < kRowsMaxAutoN && ns < kRowsMaxAutoN) {
+            path = NBODY_PATH_ROWS;   // a forced variant is the row-split path's
         } else if (all_pairs && nt >= kSymMinN &&
                    plan_sym(nt, sm, occ.sym[auto_sym_variant(nt)], auto_sym_variant(nt), o.splits,
                             o.dists, budget, p)) {
@@ -599,6 +722,13 @@ nbody_status make_plan_uncached(int64_t nt, int64_t ns, bool all_pairs, int sm,
         return plan_sym(nt, sm, occ.sym[variant], variant, o.splits, o.dists, budget, p)
                    ? NBODY_OK
                    : NBODY_ERR_WORKSPACE;
+    }
+    if (path == NBODY_PATH_ROWS) {
+        if (o.variant >= nbody::rows_variant_count()) return NBODY_ERR_INVALID_ARG;
+        // sources (or piece sums) beyond shared memory
+        const bool ok = o.variant < 0 ? plan_rows_auto(nt, ns, sm, o.splits, p)
+                                      : plan_rows(nt, ns, sm, o.variant, o.splits, p);
+        return ok ? NBODY_OK : NBODY_ERR_INVALID_ARG;
     }
     if (path == NBODY_PATH_TILED) {
         const int variant = o.variant < 0 ? auto_tiled_variant(nt, ns, all_pairs) : o.variant;
@@ -630,7 +760,7 @@ nbody_status make_plan(int64_t nt, int64_t ns, bool all_pairs, int sm, const Occ
     nbody_forces_opts o = {NBODY_PATH_AUTO, -1, 0, NBODY_PRECISION_DEFAULT,
                            NBODY_QUANTITIES_ACC_POT, 0};
     if (opts != nullptr) o = *opts;
-    if (o.path < NBODY_PATH_AUTO || o.path > NBODY_PATH_SYMMETRIC || o.splits < 0 || o.dists < 0)
+    if (o.path < NBODY_PATH_AUTO || o.path > NBODY_PATH_ROWS || o.splits < 0 || o.dists < 0)
         return NBODY_ERR_INVALID_ARG;
     if (o.precision < 0 || o.precision > 1) return NBODY_ERR_INVALID_ARG;
     if (o.quantities < 0 || o.quantities > 1) return NBODY_ERR_INVALID_ARG;
@@ -693,6 +823,8 @@ cudaError_t launch_planned(const nbody_plan &plan, const nbody::Problem &pr, flo
         if (fused != nullptr) *fused = eu != nullptr;
         return cudaSuccess;
     }
+    if (plan.path == NBODY_PATH_ROWS)
+        return nbody::launch_rows(plan.variant, pr, rows_launch(plan), out, stream);
     const int ntiles = static_cast<int>(ceil_div(pr.ns, plan.tile));
     if (plan.path == NBODY_PATH_CLUSTER)
         return nbody::launch_cluster(plan.variant, pr, plan.num_iblocks, plan.cluster,
@@ -885,6 +1017,22 @@ cudaError_t capture_graph(cudaStream_t cap, Body body, cudaGraphExec_t *exec) {
     return e;
 }
 
+// Small-N paths, whose force kernel can apply the Euler step as it stores
+// each body's result (into a second position buffer).
+bool fuses_euler(const nbody_plan &plan) {
+    return plan.path == NBODY_PATH_CLUSTER || plan.path == NBODY_PATH_ROWS;
+}
+
+// The force kernel of a small-N plan with the Euler step fused.
+cudaError_t launch_fused(const nbody_plan &plan, const nbody::Problem &pr, float4 *acc,
+                         const nbody::EulerFuse &eu, cudaStream_t s) {
+    if (plan.path == NBODY_PATH_ROWS)
+        return nbody::launch_rows(plan.variant, pr, rows_launch(plan), acc, s, &eu);
+    const int ntiles = static_cast<int>(ceil_div(pr.ns, plan.tile));
+    return nbody::launch_cluster(plan.variant, pr, plan.num_iblocks, plan.cluster,
+                                 plan.tiles_per_split, ntiles, acc, s, &eu);
+}
+
 // The plan of one simulation step and the workspace it needs (the plan's
 // partials, then at small n the second position buffer).
 nbody_status sim_plan(DeviceState *dev, int64_t n, int64_t budget, nbody_plan *plan,
@@ -892,7 +1040,7 @@ nbody_status sim_plan(DeviceState *dev, int64_t n, int64_t budget, nbody_plan *p
     nbody_status st = make_plan(n, n, true, dev->sm_count, device_occupancy(dev), nullptr, budget,
                                 plan, dev);
     if (st != NBODY_OK) return st;
-    *bytes = plan->scratch_bytes + (plan->path == NBODY_PATH_CLUSTER ? 16 * n : 0);
+    *bytes = plan->scratch_bytes + (fuses_euler(*plan) ? 16 * n : 0);
     return NBODY_OK;
 }
 
@@ -958,21 +1106,19 @@ nbody_status sim_build(int dev_id, DeviceState *dev, const SimKey &k, SimGraph &
         return launch_step(plan, pr, acc, parts, dev->sm_count, pos, vel, k.dt, s);
     }, &exec);
     // Small N: two steps per replay with the Euler update fused into the
-    // cluster kernel, positions alternating between pos_mass and pos_b.
-    if (e == cudaSuccess && plan.path == NBODY_PATH_CLUSTER && ws != nullptr &&
-        room >= plan.scratch_bytes + 16 * k.n) {
-        float4 *pb = reinterpret_cast<float4 *>(static_cast<char *>(ws) + plan.scratch_bytes);
-        const nbody::Problem pr_b = {reinterpret_cast<const float *>(pb),
-                                     reinterpret_cast<const float *>(pb), ni, ni, k.eps2, true};
-        const int ntiles = static_cast<int>(ceil_div(k.n, plan.tile));
-        const nbody::EulerFuse to_b = {pb, vel, k.dt};
-        const nbody::EulerFuse to_a = {pos, vel, k.dt};
+    // force kernel, positions alternating between pos_mass and pos_b.
+    float4 *pb = nullptr;
+    if (e == cudaSuccess && fuses_euler(plan) && ws != nullptr &&
+        room >= plan.scratch_bytes + 16 * k.n)
+        pb = reinterpret_cast<float4 *>(static_cast<char *>(ws) + plan.scratch_bytes);
+    const nbody::Problem pr_b = {reinterpret_cast<const float *>(pb),
+                                 reinterpret_cast<const float *>(pb), ni, ni, k.eps2, true};
+    const nbody::EulerFuse to_b = {pb, vel, k.dt};
+    const nbody::EulerFuse to_a = {pos, vel, k.dt};
+    if (pb != nullptr) {
         e = capture_graph(cap, [&](cudaStream_t s) {
-            cudaError_t el = nbody::launch_cluster(plan.variant, pr, plan.num_iblocks, plan.cluster,
-                                                   plan.tiles_per_split, ntiles, acc, s, &to_b);
-            if (el == cudaSuccess)
-                el = nbody::launch_cluster(plan.variant, pr_b, plan.num_iblocks, plan.cluster,
-                                           plan.tiles_per_split, ntiles, acc, s, &to_a);
+            cudaError_t el = launch_fused(plan, pr, acc, to_b, s);
+            if (el == cudaSuccess) el = launch_fused(plan, pr_b, acc, to_a, s);
             return el;
         }, &exec2);
     }
@@ -982,21 +1128,11 @@ nbody_status sim_build(int dev_id, DeviceState *dev, const SimKey &k, SimGraph &
     cudaGraphExec_t execb = nullptr;
     if (e == cudaSuccess && k.n <= kSimBatchMaxN) {
         if (exec2 != nullptr) {
-            float4 *pb = reinterpret_cast<float4 *>(static_cast<char *>(ws) + plan.scratch_bytes);
-            const nbody::Problem pr_b = {reinterpret_cast<const float *>(pb),
-                                         reinterpret_cast<const float *>(pb), ni, ni, k.eps2, true};
-            const int ntiles = static_cast<int>(ceil_div(k.n, plan.tile));
-            const nbody::EulerFuse to_b = {pb, vel, k.dt};
-            const nbody::EulerFuse to_a = {pos, vel, k.dt};
             e = capture_graph(cap, [&](cudaStream_t s) {
                 cudaError_t el = cudaSuccess;
                 for (int t = 0; t < kSimBatch / 2 && el == cudaSuccess; ++t) {
-                    el = nbody::launch_cluster(plan.variant, pr, plan.num_iblocks, plan.cluster,
-                                               plan.tiles_per_split, ntiles, acc, s, &to_b);
-                    if (el == cudaSuccess)
-                        el = nbody::launch_cluster(plan.variant, pr_b, plan.num_iblocks,
-                                                   plan.cluster, plan.tiles_per_split, ntiles, acc,
-                                                   s, &to_a);
+                    el = launch_fused(plan, pr, acc, to_b, s);
+                    if (el == cudaSuccess) el = launch_fused(plan, pr_b, acc, to_a, s);
                 }
                 return el;
             }, &execb);
@@ -1072,8 +1208,9 @@ int nominal_occ(int i_per_thread, int threads) {
     return occ < 1 ? 1 : occ;
 }
 
-nbody_status host_plan(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
-                       const nbody_forces_opts *opts, int64_t budget, nbody_plan *plan) {
+nbody_status host_plan(int64_t nt, int64_t ns, bool all_pairs, int32_t sm_count,
+                       int32_t ctas_per_sm, const nbody_forces_opts *opts, int64_t budget,
+                       nbody_plan *plan) {
     int occ[kMaxVariants], cocc[kMaxVariants], socc[kMaxVariants];
     for (int v = 0; v < nbody::tiled_variant_count() && v < kMaxVariants; ++v) {
         const nbody::TiledVariant &tv = nbody::tiled_variant(v);
@@ -1088,7 +1225,7 @@ nbody_status host_plan(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
         const int by_smem = static_cast<int>(kSmemPerSm / static_cast<int64_t>(sv.smem + 1024));
         socc[v] = ctas_per_sm > 0 ? ctas_per_sm : std::max(1, std::min(sv.min_ctas, by_smem));
     }
-    return make_plan(n, n, true, sm_count, Occupancy{occ, cocc, socc}, opts, budget, plan);
+    return make_plan(nt, ns, all_pairs, sm_count, Occupancy{occ, cocc, socc}, opts, budget, plan);
 }
 
 nbody_forces_opts with_quantities(const nbody_forces_opts *opts, int quantities) {
@@ -1175,14 +1312,22 @@ int nbody_last_cuda_error(void) { return g_last_cuda_error; }
 
 nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
                                const nbody_forces_opts *opts, nbody_plan *plan) {
-    return host_plan(n, sm_count, ctas_per_sm, opts, n > 0 ? pool_budget(n) : 0, plan);
+    return host_plan(n, n, true, sm_count, ctas_per_sm, opts, n > 0 ? pool_budget(n) : 0, plan);
 }
 
 nbody_status nbody_plan_forces_ws(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
                                   const nbody_forces_opts *opts, int64_t workspace_bytes,
                                   nbody_plan *plan) {
     if (workspace_bytes < 0) return NBODY_ERR_INVALID_ARG;
-    return host_plan(n, sm_count, ctas_per_sm, opts, workspace_bytes, plan);
+    return host_plan(n, n, true, sm_count, ctas_per_sm, opts, workspace_bytes, plan);
+}
+
+nbody_status nbody_plan_forces_ts(int64_t nt, int64_t ns, int32_t sm_count, int32_t ctas_per_sm,
+                                  const nbody_forces_opts *opts, int64_t workspace_bytes,
+                                  nbody_plan *plan) {
+    if (workspace_bytes < -1) return NBODY_ERR_INVALID_ARG;
+    return host_plan(nt, ns, false, sm_count, ctas_per_sm, opts,
+                     workspace_bytes >= 0 ? workspace_bytes : (nt > 0 ? pool_budget(nt) : 0), plan);
 }
 
 nbody_status nbody_forces_ex(const float *pos_mass, int64_t n, float eps2, float *acc_pot,

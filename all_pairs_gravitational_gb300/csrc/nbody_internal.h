@@ -101,6 +101,45 @@ cudaError_t launch_cluster(int variant, const Problem &pr, int num_ib, int clust
                            int tiles_per_cta, int ntiles, float4 *out, cudaStream_t stream,
                            const EulerFuse *euler = nullptr);
 
+// The row-split kernel's decomposition: CTA b takes targets [b tb, (b + 1) tb)
+// (fewer in the last CTA); its warp items are `groups` runs of K targets
+// (tb_pad = groups K >= tb) times `pieces` pieces of `cols` source pairs each
+// (cols a multiple of 32; ns_pad = 2 pieces cols >= ns, zero past ns).
+struct RowsLaunch {
+    int tb;
+    int groups;
+    int tb_pad;
+    int pieces;
+    int cols;
+    int ns_pad;
+};
+
+// A compiled instantiation of the row-split kernel.
+struct RowsVariant {
+    int i_per_warp;       // K targets per warp item
+    int warps;            // W warps per CTA
+    const void *fn_pot;   // a and p
+    const void *fn_acc;   // a only
+    const void *fn_pot_euler;   // the same with the Euler step fused
+    const void *fn_acc_euler;
+    cudaError_t (*launch)(const struct Problem &, const struct RowsLaunch &, float4 *,
+                          cudaStream_t, const struct EulerFuse *);
+};
+
+int rows_variant_count();
+const RowsVariant &rows_variant(int v);
+
+// Dynamic shared memory of a row-split launch: the sources and the piece sums.
+size_t rows_smem_bytes(int ns_pad, int pieces, int tb_pad);
+
+// Largest dynamic shared memory of a row-split CTA (the sm_103 opt-in limit
+// of 227 KB per block).
+constexpr size_t kRowsSmemMax = 227 * 1024;
+
+// Row-split kernel over ceil(nt / tb) CTAs; writes out[i] directly.
+cudaError_t launch_rows(int variant, const Problem &pr, const RowsLaunch &rl, float4 *out,
+                        cudaStream_t stream, const EulerFuse *euler = nullptr);
+
 // A compiled instantiation of the symmetric (each unordered pair once) kernel.
 struct SymVariant {
     int i_per_thread;   // K targets per lane (even)

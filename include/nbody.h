@@ -214,9 +214,24 @@ enum {
     NBODY_PATH_AUTO = 0,     /* the library's choice from n and the SM count */
     NBODY_PATH_TILED = 1,    /* i-blocks x j-splits over the whole grid (any n) */
     NBODY_PATH_CLUSTER = 2,  /* small n: warps and a CTA cluster split j, DSMEM reduction */
-    NBODY_PATH_SYMMETRIC = 3 /* all-pairs only: each unordered pair evaluated once and
+    NBODY_PATH_SYMMETRIC = 3,/* all-pairs only: each unordered pair evaluated once and
                                 applied to both bodies (see below) */
+    NBODY_PATH_ROWS = 4      /* few sources: each target's row split over the lanes of a
+                                warp, every source in shared memory (see below) */
 };
+
+/*
+ * The row-split path.  Below about ten thousand bodies one thread per target
+ * leaves most of the GPU idle; the GPU Gems 3 ch.31 study page (section 4)
+ * splits a body's row over several threads instead.  One CTA per SM takes
+ * ceil(nt / SMs) consecutive targets and stages every source into shared
+ * memory (so ns is limited to about 14000 sources: NBODY_ERR_INVALID_ARG
+ * beyond).  A warp takes K targets against one of S pieces of at most 2048
+ * sources, its lanes striding over the piece two sources per f32x2
+ * operation; each target's lane sums are added by a fixed shuffle tree and
+ * its S piece sums in order, compensated.  No workspace, no atomics:
+ * deterministic.  opts.splits forces S.
+ */
 
 /*
  * The symmetric path.  The pull of j on i and of i on j share r, |r|^2 + eps^2
@@ -242,8 +257,9 @@ enum {
 typedef struct nbody_forces_opts {
     int32_t path;       /* NBODY_PATH_* */
     int32_t variant;    /* kernel variant of the path; -1 = library default */
-    int32_t splits;     /* tiled path: pieces S of the source range; symmetric path:
-                           pieces P of a row per group (0 = planner's choice) */
+    int32_t splits;     /* tiled and row-split paths: pieces S of the source range;
+                           symmetric path: pieces P of a row per group (0 = planner's
+                           choice) */
     int32_t precision;  /* NBODY_PRECISION_* */
     int32_t quantities; /* NBODY_QUANTITIES_* */
     int32_t dists;      /* symmetric path: distances D per group (0 = planner's choice) */
@@ -268,16 +284,19 @@ enum {
 
 /* The decomposition nbody_forces would launch; host-only, needs no GPU. */
 typedef struct nbody_plan {
-    int32_t path;            /* NBODY_PATH_TILED, _CLUSTER or _SYMMETRIC */
+    int32_t path;            /* NBODY_PATH_TILED, _CLUSTER, _SYMMETRIC or _ROWS */
     int32_t variant;         /* kernel variant index of that path */
-    int32_t i_per_thread;    /* target bodies held in registers by each thread */
+    int32_t i_per_thread;    /* target bodies held in registers by each thread (row-split:
+                                by each warp item) */
     int32_t threads;         /* threads per CTA computing pairs */
-    int32_t tile;            /* source bodies per shared-memory tile (symmetric: per unit) */
+    int32_t tile;            /* source bodies per shared-memory tile (symmetric: per unit;
+                                row-split: per piece, padded) */
     int32_t num_iblocks;     /* CTAs along the targets (symmetric: the nb blocks) */
-    int32_t splits;          /* tiled: pieces S of the source range; symmetric: pieces P
-                                of a row per group; cluster: CTAs x warps splitting j */
+    int32_t splits;          /* tiled, row-split: pieces S of the source range; symmetric:
+                                pieces P of a row per group; cluster: CTAs x warps
+                                splitting j */
     int32_t tiles_per_split; /* tiled: source tiles per piece; symmetric: units of
-                                the largest piece */
+                                the largest piece; row-split: targets per CTA */
     int32_t cluster;         /* cluster path: CTAs per cluster */
     int32_t warps_j;         /* cluster path: warps splitting j inside a CTA */
     int32_t dists;           /* symmetric: distances D per group; 0 otherwise */
@@ -303,6 +322,14 @@ nbody_status nbody_plan_forces(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
 /* nbody_plan_forces within a workspace of `workspace_bytes` (>= 0).  Errors:
  * NBODY_ERR_INVALID_ARG; NBODY_ERR_WORKSPACE if a forced path cannot run in it. */
 nbody_status nbody_plan_forces_ws(int64_t n, int32_t sm_count, int32_t ctas_per_sm,
+                                  const nbody_forces_opts *opts, int64_t workspace_bytes,
+                                  nbody_plan *plan);
+
+/* The plan of nbody_forces_ts for nt targets and ns sources held in separate
+ * arrays (the symmetric path is not open to it), within `workspace_bytes`
+ * (>= 0), or the default budget for -1.  Host only.  Errors:
+ * NBODY_ERR_INVALID_ARG; NBODY_ERR_WORKSPACE if a forced path cannot run in it. */
+nbody_status nbody_plan_forces_ts(int64_t nt, int64_t ns, int32_t sm_count, int32_t ctas_per_sm,
                                   const nbody_forces_opts *opts, int64_t workspace_bytes,
                                   nbody_plan *plan);
 

@@ -8,6 +8,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import all_pairs_gravitational_gb300 as apg
@@ -137,6 +138,9 @@ def _covers(plan, n, budget=None):
     if plan["path"] == apg.NBODY_PATH_SYMMETRIC:
         _sym_covers(plan, n)
         return
+    if plan["path"] == apg.NBODY_PATH_ROWS:
+        _rows_covers(plan, n, n)
+        return
     if plan["path"] == apg.NBODY_PATH_TILED:
         bi = plan["threads"] * plan["i_per_thread"]
         tps, s = plan["tiles_per_split"], plan["splits"]
@@ -164,6 +168,71 @@ def _covers(plan, n, budget=None):
     assert s * tps >= ntiles > (s - 1) * tps
     assert plan["grid"] < 2 ** 31
     assert 0 < plan["fill"] <= 1.0
+
+
+def _rows_items(plan, nt, ns):
+    """The warp items of a row-split plan, as the header states them: CTA b
+    takes targets [b tb, (b + 1) tb); its items are runs of K of them (the
+    last run of a CTA may be short) against S pieces of `tile` sources."""
+    tb, k, s, tile = (plan["tiles_per_split"], plan["i_per_thread"], plan["splits"],
+                      plan["tile"])
+    for b in range(plan["num_iblocks"]):
+        t0, t1 = b * tb, min((b + 1) * tb, nt)
+        for g in range(0, t1 - t0, k):
+            for piece in range(s):
+                yield (range(t0 + g, min(t0 + g + k, t1)),
+                       range(piece * tile, min((piece + 1) * tile, ns)))
+
+
+def _rows_covers(plan, nt, ns, sm=None):
+    tb = plan["tiles_per_split"]
+    assert plan["i_per_thread"] in (7, 6, 4, 2) and plan["threads"] in (256, 384)
+    assert plan["num_iblocks"] == plan["grid"] == -(-nt // tb)
+    if sm is not None:   # an equal share of the targets per SM
+        assert tb == -(-nt // sm) and plan["grid"] <= sm
+    assert plan["tile"] % 64 == 0 and plan["splits"] * plan["tile"] >= ns
+    assert plan["scratch_bytes"] == plan["scratch_min_bytes"] == 0 and plan["passes"] == 1
+    assert 0 < plan["fill"] <= 1.0
+    # shared memory: the padded sources and the piece sums of the CTA's targets
+    tb_pad = -(-tb // plan["i_per_thread"]) * plan["i_per_thread"]
+    assert 16 * plan["splits"] * plan["tile"] + 16 * plan["splits"] * tb_pad <= 227 * 1024
+
+
+@pytest.mark.parametrize("nt,ns", [(1, 1), (2, 2), (3, 3), (33, 33), (152, 152), (153, 153),
+                                   (1000, 1000), (1024, 1024), (2047, 2047), (300, 5000),
+                                   (5000, 300), (4097, 4097)])
+def test_rows_decomposition_meets_every_pair_once(nt, ns):
+    plan = apg.nbody_plan_forces_ts(nt, ns, 152, path=apg.NBODY_PATH_ROWS)
+    _rows_covers(plan, nt, ns, 152)
+    seen = np.zeros((nt, ns), dtype=np.int32)
+    for ti, sj in _rows_items(plan, nt, ns):
+        if len(ti) and len(sj):
+            seen[ti.start:ti.stop, sj.start:sj.stop] += 1
+    assert (seen == 1).all()
+
+
+@pytest.mark.parametrize("n", [1, 7, 1000, 1024, 2048, 3072, 4096, 4864, 6144, 8192, 10239])
+def test_rows_plan_bounds(n):
+    """Automatic row-split plans: at most 2048 sources per piece (32 terms
+    per lane half before the tree), and forced variants and piece counts are
+    honoured."""
+    plan = apg.nbody_plan_forces(n, 152)
+    assert plan["path"] == apg.NBODY_PATH_ROWS and plan["tile"] <= 2048
+    _rows_covers(plan, n, n, 152)
+    for v in range(4):
+        forced = apg.nbody_plan_forces(n, 152, path=apg.NBODY_PATH_ROWS, variant=v)
+        assert forced["variant"] == v
+        _rows_covers(forced, n, n)
+    three = apg.nbody_plan_forces(n, 152, path=apg.NBODY_PATH_ROWS, splits=3)
+    assert three["splits"] == 3
+    _rows_covers(three, n, n)
+
+
+def test_rows_plan_rejects_sources_beyond_shared_memory():
+    with pytest.raises(apg.NbodyError):
+        apg.nbody_plan_forces(20000, 152, path=apg.NBODY_PATH_ROWS)
+    # the automatic choice then takes another path
+    assert apg.nbody_plan_forces_ts(100, 20000, 152)["path"] == apg.NBODY_PATH_TILED
 
 
 def _sym_units(nb):
@@ -419,11 +488,13 @@ def test_cluster_plan_covers_all_pairs(n, variant):
 
 
 def test_auto_path_choice():
-    assert apg.nbody_plan_forces(1024, 152)["path"] == apg.NBODY_PATH_CLUSTER
-    assert apg.nbody_plan_forces(4096, 152)["path"] == apg.NBODY_PATH_CLUSTER
-    assert apg.nbody_plan_forces(8192, 152)["path"] == apg.NBODY_PATH_TILED
-    assert apg.nbody_plan_forces(10239, 152)["path"] == apg.NBODY_PATH_TILED
+    for n in (1, 1024, 4096, 4864, 8192, 10239):
+        assert apg.nbody_plan_forces(n, 152)["path"] == apg.NBODY_PATH_ROWS
     assert apg.nbody_plan_forces(10240, 152)["path"] == apg.NBODY_PATH_SYMMETRIC
+    # the row-split variant by the cost model, the measured fastest: K = 7, except
+    # K = 4 (12 warps) at 4864
+    assert [apg.nbody_plan_forces(n, 152)["i_per_thread"] for n in (1024, 4096, 4864, 8192)] == \
+        [7, 7, 4, 7]
     # the symmetric block size grows with n: 512, 1024, then 2048 bodies
     blocks = [apg.nbody_plan_forces(n, 152)["threads"] * apg.nbody_plan_forces(n, 152)["i_per_thread"]
               for n in (10240, 45055, 45056, 163839, 163840, 1048576)]

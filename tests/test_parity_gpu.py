@@ -243,7 +243,7 @@ def test_forced_plans(variant, splits):
     assert_parity(got, ref)
 
 
-@pytest.mark.parametrize("path", [1, 2, 3])
+@pytest.mark.parametrize("path", [1, 2, 3, 4])
 def test_disk_near_neighbours_all_paths(path):
     """The disk workload has bodies whose nearest neighbours contribute terms
     hundreds of times |a_i| (condition number ~1e3): the per-body bound holds."""
@@ -261,11 +261,58 @@ def test_cluster_path(variant, n):
 
 
 def test_paths_agree_small_n():
-    """Both paths on the same input: each within tolerance of the oracle."""
+    """Every small-N path on the same input: each within tolerance of the oracle."""
     w = W.small_cube(2048)
     ref = oracle.forces(w.pos_mass, w.eps2)
-    for path in (apg.NBODY_PATH_TILED, apg.NBODY_PATH_CLUSTER):
+    for path in (apg.NBODY_PATH_TILED, apg.NBODY_PATH_CLUSTER, apg.NBODY_PATH_ROWS):
         assert_parity(gpu_forces(w.pos_mass, w.eps2, path=path), ref)
+
+
+# ------------------------------------------------------------ row-split path
+
+ROWS = apg.NBODY_PATH_ROWS
+
+
+@pytest.mark.parametrize("variant", range(_variant_count(ROWS)))
+@pytest.mark.parametrize("n", [1, 2, 3, 7, 100, 152, 153, 1000, 1064, 2048, 3071, 4096, 4865,
+                               8192, 10239, 12000])
+def test_rows_path(variant, n):
+    """Each row-split shape on ragged sizes: targets per CTA not a multiple
+    of K (phantom targets), sources not a multiple of 64 (zero padding),
+    one to several pieces."""
+    w = W.cube(n, seed=n + 11)
+    got = gpu_forces(w.pos_mass, w.eps2, path=ROWS, variant=variant)
+    assert_parity(got, oracle.forces(w.pos_mass, w.eps2))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 40])
+def test_rows_forced_pieces(splits):
+    """Forced piece counts, including pieces longer than 2048 sources and
+    pieces made only of padding."""
+    w = W.clumps(5003, seed=78)
+    got = gpu_forces(w.pos_mass, w.eps2, path=ROWS, splits=splits)
+    assert_parity(got, oracle.forces(w.pos_mass, w.eps2))
+
+
+def test_rows_path_deterministic_and_the_automatic_choice():
+    w = W.small_cube(4096)
+    a = gpu_forces(w.pos_mass, w.eps2, path=ROWS)
+    for _ in range(3):
+        assert np.array_equal(gpu_forces(w.pos_mass, w.eps2, path=ROWS), a)
+    assert np.array_equal(gpu_forces(w.pos_mass, w.eps2), a)
+
+
+@pytest.mark.parametrize("nt,ns", [(1, 1), (1, 5000), (5000, 1), (37, 10000), (10000, 37),
+                                   (700, 4099), (20000, 3000)])
+def test_rows_target_source_form(nt, ns):
+    """Separate target and source arrays: few sources against few or many
+    targets (20000 targets: several items per warp)."""
+    t, s = _ts_bodies(nt, ns, nt * 5 + ns)
+    eps2 = np.float32(1e-3)
+    out = apg.nbody_forces_ts_ws(torch.from_numpy(t).to(dev()), torch.from_numpy(s).to(dev()),
+                                 float(eps2), workspace=torch.empty(0, device=dev()), path=ROWS)
+    torch.cuda.synchronize()
+    assert_parity(out.cpu().numpy(), oracle.forces_ts(t, s, eps2))
 
 
 def test_cluster_path_deterministic():
@@ -534,7 +581,7 @@ def _separate_steps(w, steps):
                                         ("cube16384", 17), ("plummer65536", 10),
                                         ("clumps200003", 2)])
 def test_simulate_is_the_separate_calls(name, steps):
-    """Cluster path (fused pairs of steps), tiled path (8192) and symmetric
+    """Row-split path (1024, 4096, 8192: fused pairs of steps) and symmetric
     path (16384, 65536, 200003); 37, 33 and 17 steps run through the
     16-step batch graph and then the pair and single-step graphs."""
     w = W.named(name)
@@ -689,11 +736,13 @@ def test_disk4096_acceleration_only():
     assert_parity(got, oracle.forces(w.pos_mass, w.eps2), potential=False)
 
 
-@pytest.mark.parametrize("path", [1, 2, 3])
+@pytest.mark.parametrize("path", [1, 2, 3, 4])
 @pytest.mark.parametrize("n", [1, 1000, 5003, 20011])
 def test_acceleration_only_every_path(path, n):
     """Each kernel without its potential operations: the acceleration is the
     same arithmetic, so it matches the a + p call bit for bit; .w is 0."""
+    if path == 4 and n > 12000:   # the row-split path holds every source in shared memory
+        n = 12000
     w = W.clumps(n, seed=n + 5)
     if path == 2 and n > 4864:
         path = 1

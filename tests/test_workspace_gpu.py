@@ -67,7 +67,7 @@ def test_size_query_is_the_default_plan(n):
     assert apg.nbody_forces_workspace_bytes(n) == plan["scratch_bytes"]
     assert plan["scratch_bytes"] <= apg.NBODY_DEFAULT_WORKSPACE_BYTES
     sim = apg.nbody_simulate_workspace_bytes(n)
-    extra = 16 * n if plan["path"] == apg.NBODY_PATH_CLUSTER else 0
+    extra = 16 * n if plan["path"] in (apg.NBODY_PATH_CLUSTER, apg.NBODY_PATH_ROWS) else 0
     assert sim == plan["scratch_bytes"] + extra
 
 
@@ -124,8 +124,9 @@ def test_no_workspace_runs_without_partials(n):
     pm = torch.from_numpy(w.pos_mass).to(dev())
     out = apg.nbody_forces_ws(pm, float(w.eps2), workspace=torch.empty(0, device=dev()))
     torch.cuda.synchronize()
-    ref = apg.nbody_forces_ex(pm, float(w.eps2), path=apg.NBODY_PATH_TILED if n > 4864 else 0,
-                              splits=1 if n > 4864 else 0)
+    # below 10240 bodies the automatic choice (row-split) has no partials anyway
+    ref = apg.nbody_forces_ex(pm, float(w.eps2), path=apg.NBODY_PATH_TILED if n >= 10240 else 0,
+                              splits=1 if n >= 10240 else 0)
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
     rows = rows_of(n, 1000, 6)
@@ -268,11 +269,11 @@ def _random_cases(count=24, seed=2024):
     cases = []
     for k in range(count):
         n = int(rng.integers(1, 30000))
-        path = int(rng.choice([0, 1, 2, 3]))
-        if path == 2 and n > 12000:
+        path = int(rng.choice([0, 1, 2, 3, 4]))
+        if path in (2, 4) and n > 12000:   # the cluster and row-split paths serve small n
             path = 0
         dists = int(rng.choice([0, 1, 2, 5])) if path == 3 else 0
-        splits = int(rng.choice([0, 1, 3, 17])) if path in (1, 3) else 0
+        splits = int(rng.choice([0, 1, 3, 17])) if path in (1, 3, 4) else 0
         cases.append((k, n, path, dists, splits))
     return cases
 
