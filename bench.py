@@ -34,8 +34,10 @@ FP32_OPS_PER_PAIR = 13        # fp32 lane operations of the pair law for one ord
 SYM_OPS_PER_PAIR = 18         # fp32 lane operations for one unordered pair, both bodies' a + p
 FP32_LANES_PER_SM_CLK = 128
 RECIPE_SM_MAX_MHZ = 2070.0    # fallback if no measured peaks file is present
+PATH_CLUSTER = 2
 PATH_SYMMETRIC = 3
-PATH_NAMES = {1: "tiled", 2: "cluster", 3: "symmetric"}
+PATH_ROWS = 4
+PATH_NAMES = {1: "tiled", 2: "cluster", 3: "symmetric", 4: "rows"}
 ACC_ONLY_WORKLOADS = {"disk4096"}   # configurations that check the acceleration only
 PATH_IDS = {"auto": 0, "tiled": 1, "symmetric": 3}
 
@@ -48,6 +50,10 @@ KERNEL_SOURCES = {
               "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"],
     "symmetric": ["all_pairs_gravitational_gb300/csrc/forces_sym.cu",
                   "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"],
+    "rows": ["all_pairs_gravitational_gb300/csrc/forces_rows.cu",
+             "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"],
+    "cluster": ["all_pairs_gravitational_gb300/csrc/forces_cluster.cu",
+                "all_pairs_gravitational_gb300/csrc/nbody_device.cuh"],
 }
 TRAFFIC_BY_SOURCE = {
     # one nbody_forces call = 7 passes of the symmetric kernel (default plan)
@@ -120,8 +126,8 @@ def euler_hbm_probe(apg, device, n=1 << 26, reps=5):
 def force_roofline(plan, n, sm, sm_max_mhz, acc_only=False):
     """Arithmetic bound of the planned force kernel, in interactions/s.
 
-    Ordered-pair kernels (tiled, cluster) execute 13 fp32 lane operations per
-    interaction.  The symmetric kernel executes 18 per unordered pair, which
+    Ordered-pair kernels (tiled, cluster, row-split) execute 13 fp32 lane
+    operations per interaction.  The symmetric kernel executes 18 per unordered pair, which
     serves two interactions, except on the nb diagonal blocks, which it
     evaluates one way (13 per ordered pair).  The bound is the FMA pipe's
     lane rate over the launch's lane operations, times its N^2 interactions."""
@@ -136,6 +142,12 @@ def force_roofline(plan, n, sm, sm_max_mhz, acc_only=False):
         diag = float((nb - 1) * t * t + last * last)
         ops = unordered / 2.0 * (pairs - diag) + ordered * diag
         kind, kernel = "symmetric", "forces_sym_kernel (+ reduce_pass_kernel)"
+    elif plan["path"] == PATH_ROWS:
+        ops = ordered * pairs
+        kind, kernel = "rows", "forces_rows_kernel"
+    elif plan["path"] == PATH_CLUSTER:
+        ops = ordered * pairs
+        kind, kernel = "cluster", "forces_cluster_kernel"
     else:
         ops = ordered * pairs
         kind, kernel = "tiled", "forces_tiled_kernel (+ reduce_pass_kernel)"
