@@ -180,6 +180,14 @@ forces_rows_kernel(const Problem pr, const RowsLaunch rl, float4 *__restrict__ o
         for (int k = 0; k < K; ++k) tgt[k] = __ldg(t4 + min(g * K + k, tb - 1));
     }
     RowItem<K, U, POT> acc;
+    // nbody_simulate: the position and velocity of the first target this
+    // thread finishes, requested now so that the Euler step at the end does
+    // not wait for them
+    float4 x_pre = make_float4(0.f, 0.f, 0.f, 0.f), v_pre = x_pre;
+    if (EULER && tid < tb) {
+        x_pre = __ldg(t4 + tid);
+        v_pre = eu.vel[t0 + tid];
+    }
 
     // every source into the four arrays (zero past ns), then the warps'
     // items in turn
@@ -216,8 +224,8 @@ forces_rows_kernel(const Problem pr, const RowsLaunch rl, float4 *__restrict__ o
         const int64_t i = t0 + t;
         out[i] = a;
         if (EULER) {   // the step of euler.cu, on this body, positions first
-            float4 x = __ldg(t4 + t);
-            float4 v = eu.vel[i];
+            float4 x = t == tid ? x_pre : __ldg(t4 + t);
+            float4 v = t == tid ? v_pre : eu.vel[i];
             euler_body(x, v, a, eu.dt);
             eu.pos_out[i] = x;
             eu.vel[i] = v;
