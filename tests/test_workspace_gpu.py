@@ -190,6 +190,24 @@ def test_simulate_ws_is_the_separate_calls(name, steps):
     apg.nbody_release_cached()      # the graph no longer refers to ws
 
 
+@pytest.mark.parametrize("name,steps", [("smallcube2048", 5), ("smallcube4096", 18)])
+def test_simulate_ws_without_room_for_the_fused_steps(name, steps):
+    """A workspace too small for the second position buffer: the row-split
+    path's steps run as a force launch and an Euler launch each (no fused
+    pairs), with the same bits as the separate calls."""
+    w = W.named(name)
+    assert apg.nbody_simulate_workspace_bytes(w.n) == 16 * w.n
+    ref = _separate_steps(w, steps)
+    pm = torch.from_numpy(w.pos_mass).to(dev())
+    vel = torch.from_numpy(w.vel).to(dev())
+    acc = torch.empty_like(pm)
+    apg.nbody_simulate_ws(pm, vel, acc, float(w.eps2), float(w.dt), steps, workspace(16))
+    torch.cuda.synchronize()
+    for got, exp in zip((pm, vel, acc), ref):
+        assert torch.equal(got, exp)
+    apg.nbody_release_cached()
+
+
 def test_simulate_same_problem_from_two_streams():
     """Two streams replay the same cached graph back to back without any
     host synchronisation: the library orders the second call after the
