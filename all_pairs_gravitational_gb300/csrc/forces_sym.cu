@@ -309,7 +309,11 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
 //   chunk): 6 % slower with the potential, equal without it;
 //   the potential terms or the j-side sums as scalar fp32 FMAs (6-10 %
 //   slower: packed f32x2 instructions occupy both halves of the FMA pipe, so
-//   no half is left idle for scalar work).
+//   no half is left idle for scalar work);
+//   each source's packed j-side sum carried round the warp with it (lane
+//   l + 1 takes it after lane l's FMAs), which removes the 8 scalar adds per
+//   step for 4 more shuffles: 2.3 % slower at 2^20 (3.3 % without the
+//   potential).
 #define NBODY_SYM_LIST(X)                     \
     X(8, 8, 64, 2, 1, true)   /* 0: default */ \
     X(8, 4, 64, 4, 1, true)   /* 1 */          \
