@@ -2,6 +2,8 @@
 // range of one target block is split across the warps of a CTA and across
 // the CTAs of a thread-block cluster, and the partial sums are added back in
 // a fixed order through shared memory and distributed shared memory (DSMEM).
+// A forced path (NBODY_PATH_CLUSTER): the automatic choice takes the
+// row-split kernel (forces_rows.cu), faster at every small size.
 //
 // With one thread per target, N = 1024 bodies would occupy a few SMs of 152
 // (the GPU Gems 3 ch.31 study page, section 4, splits a body's row over

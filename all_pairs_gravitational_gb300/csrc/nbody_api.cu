@@ -938,7 +938,7 @@ nbody_status default_workspace(int64_t nt, int64_t ns, bool all_pairs,
 // internal stream and replayed `steps` times on the caller's stream, so a
 // step costs one graph launch instead of several kernel launches from the
 // host.  Where the forces end in a reduction kernel, the Euler update runs
-// inside its last pass.  On the cluster path (small N) a second graph holds
+// inside its last pass.  On the small-N paths (row-split, cluster) a second graph holds
 // two steps whose Euler update is fused into the force kernel, the positions
 // going from pos_mass to a second buffer and back; steps run in pairs
 // through it, and an odd last step through the one-step graph.  One graph

@@ -291,16 +291,18 @@ typedef struct nbody_plan {
     int32_t threads;         /* threads per CTA computing pairs */
     int32_t tile;            /* source bodies per shared-memory tile (symmetric: per unit;
                                 row-split: per piece, padded) */
-    int32_t num_iblocks;     /* CTAs along the targets (symmetric: the nb blocks) */
+    int32_t num_iblocks;     /* CTAs along the targets (symmetric: the nb blocks;
+                                row-split: the CTAs, one per SM at most) */
     int32_t splits;          /* tiled, row-split: pieces S of the source range; symmetric:
                                 pieces P of a row per group; cluster: CTAs x warps
                                 splitting j */
     int32_t tiles_per_split; /* tiled: source tiles per piece; symmetric: units of
                                 the largest piece; row-split: targets per CTA */
     int32_t cluster;         /* cluster path: CTAs per cluster */
-    int32_t warps_j;         /* cluster path: warps splitting j inside a CTA */
+    int32_t warps_j;         /* cluster path: warps splitting j inside a CTA; row-split:
+                                warps per CTA */
     int32_t dists;           /* symmetric: distances D per group; 0 otherwise */
-    int32_t groups;          /* symmetric: groups of distances; tiled: S; cluster: 1 */
+    int32_t groups;          /* symmetric: groups of distances; tiled: S; cluster, row-split: 1 */
     int32_t groups_per_pass; /* groups evaluated by one force launch */
     int32_t passes;          /* force launches (each followed by its reduction if any) */
     int64_t grid;            /* CTAs of the largest force launch */

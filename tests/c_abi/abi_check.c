@@ -101,6 +101,10 @@ int main(void) {
     if (plan.path != NBODY_PATH_SYMMETRIC || plan.scratch_bytes <= 0 ||
         plan.scratch_bytes > NBODY_DEFAULT_WORKSPACE_BYTES)
         return 13;
+    /* the target/source planner: few sources take the row-split path, with
+     * no workspace and one CTA per SM */
+    if (nbody_plan_forces_ts(3000, 500, 152, 0, &autoo, -1, &plan) != NBODY_OK) return 19;
+    if (plan.path != NBODY_PATH_ROWS || plan.scratch_bytes != 0 || plan.grid > 152) return 20;
 
     /* the symmetric path again within a caller-owned workspace: ask for its
      * size, give it exactly that, and get the same bits */
