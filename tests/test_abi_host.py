@@ -229,6 +229,11 @@ def test_rows_plan_bounds(n):
 
 
 def test_rows_plan_rejects_sources_beyond_shared_memory():
+    # every source in shared memory: up to 14400 with few targets, not 14500
+    plan = apg.nbody_plan_forces_ts(100, 14400, 152, path=apg.NBODY_PATH_ROWS)
+    _rows_covers(plan, 100, 14400, 152)
+    with pytest.raises(apg.NbodyError):
+        apg.nbody_plan_forces_ts(100, 14500, 152, path=apg.NBODY_PATH_ROWS)
     with pytest.raises(apg.NbodyError):
         apg.nbody_plan_forces(20000, 152, path=apg.NBODY_PATH_ROWS)
     # the automatic choice then takes another path

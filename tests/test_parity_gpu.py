@@ -303,10 +303,11 @@ def test_rows_path_deterministic_and_the_automatic_choice():
 
 
 @pytest.mark.parametrize("nt,ns", [(1, 1), (1, 5000), (5000, 1), (37, 10000), (10000, 37),
-                                   (700, 4099), (20000, 3000)])
+                                   (700, 4099), (20000, 3000), (100, 14400), (1000, 14000)])
 def test_rows_target_source_form(nt, ns):
     """Separate target and source arrays: few sources against few or many
-    targets (20000 targets: several items per warp)."""
+    targets (20000 targets: several items per warp), and the most sources
+    shared memory holds (14400: 225 KB per CTA)."""
     t, s = _ts_bodies(nt, ns, nt * 5 + ns)
     eps2 = np.float32(1e-3)
     out = apg.nbody_forces_ts_ws(torch.from_numpy(t).to(dev()), torch.from_numpy(s).to(dev()),
