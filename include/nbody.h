@@ -230,7 +230,9 @@ enum {
  * sources, its lanes striding over the piece two sources per f32x2
  * operation; each target's lane sums are added by a fixed shuffle tree and
  * its S piece sums in order, compensated.  No workspace, no atomics:
- * deterministic.  opts.splits forces S.
+ * deterministic.  opts.splits forces S.  The automatic choice takes it when
+ * the sources number fewer than 10240 and the targets fewer than 10240, or
+ * (separate target and source arrays) up to 131072 where its piece sums fit.
  */
 
 /*

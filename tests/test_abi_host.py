@@ -496,6 +496,12 @@ def test_auto_path_choice():
     for n in (1, 1024, 4096, 4864, 8192, 10239):
         assert apg.nbody_plan_forces(n, 152)["path"] == apg.NBODY_PATH_ROWS
     assert apg.nbody_plan_forces(10240, 152)["path"] == apg.NBODY_PATH_SYMMETRIC
+    # target/source calls: the row-split path for fewer than 10240 sources and
+    # up to 131072 targets where its piece sums fit, the tiled path otherwise
+    ts = lambda nt, ns: apg.nbody_plan_forces_ts(nt, ns, 152)["path"]
+    assert ts(20000, 1000) == ts(131072, 2000) == ts(5000, 10239) == apg.NBODY_PATH_ROWS
+    assert ts(131073, 2000) == ts(131072, 10000) == ts(100, 10240) == apg.NBODY_PATH_TILED
+    assert ts(1000000, 1000) == apg.NBODY_PATH_TILED
     # the row-split variant by the cost model, the measured fastest: K = 7, except
     # K = 4 (12 warps) at 4864
     assert [apg.nbody_plan_forces(n, 152)["i_per_thread"] for n in (1024, 4096, 4864, 8192)] == \
