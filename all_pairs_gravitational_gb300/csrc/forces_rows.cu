@@ -16,16 +16,18 @@
 //     (2c, 2c + 1) of the columns c = l, l + 32, ... of the piece: one f32x2
 //     operation serves two sources, and a warp's 8-byte loads are
 //     contiguous;
-//   * at the end of an item, each target's 64 lane sums (two per lane) are
-//     added by a fixed shuffle tree, and lane 0 stores the piece's sum in
-//     shared memory;
+//   * at the end of an item, each lane adds its two halves, and the 4 K
+//     values of the item (a and p of K targets) are added across the warp
+//     by a fixed recursive-halving shuffle exchange (warp_sum_transposed);
+//     the lanes holding the totals store the piece's sums in shared memory;
 //   * after a barrier, thread t adds target t's S piece sums in order,
 //     compensated, and stores (ax, ay, az, p); in nbody_simulate it then
 //     applies the Euler step to that body.
 // No atomics, no global scratch and no cluster: the results are
-// deterministic.  A piece holds at most 2048 sources, so a lane sums at most
-// 32 terms per half before the tree: the run length between the compensated
-// folds of the other kernels.
+// deterministic.  A piece holds at most 2048 sources (the planner's rule;
+// a forced piece count may exceed it), so a lane sums at most 32 terms per
+// half before the exchange: the run length between the compensated folds of
+// the other kernels.
 #include <algorithm>
 
 #include "nbody_device.cuh"
