@@ -292,7 +292,9 @@ forces_sym_kernel(const float4 *__restrict__ bodies, int n, float eps2, int nb, 
 // registers).
 // Measured and dropped, each relative to the best shape of its time:
 //   128-body units (1.5-2.5 % slower), 32-body units (2-3 % slower);
-//   K = 6 or 4 (6-12 % slower); K = 2 or 4 with 32-body units and 256- or
+//   K = 6 or 4 (6-12 % slower); K = 12 with 8 or 4 warps (204-228
+//   registers, 8 warps per SM: 10-11 % slower at 2^20, equal without the
+//   potential); K = 2 or 4 with 32-body units and 256- or
 //   512-body blocks (slower than variant 2 at every size from 2048 bodies);
 //   the chunk loop unrolled by 2 or 4 (2-4 % slower);
 //   each target pair's geometry and accumulation in turn (2.4 % slower);
