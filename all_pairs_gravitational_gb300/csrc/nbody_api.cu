@@ -524,6 +524,7 @@ nbody::RowsLaunch rows_launch(const nbody_plan &plan) {
 constexpr int64_t kSymMinN = 10240;
 constexpr int64_t kSymMidN = 45056;     // from here 1024-body blocks
 constexpr int64_t kSymLargeN = 163840;  // from here 2048-body blocks
+constexpr int64_t kSymFinerMinN = 16384; // finer pieces for the smaller blocks from here
 constexpr int kSymSmallVariant = 2;     // K = 8, 2 warps: 512-body blocks
 constexpr int kSymMidVariant = 1;       // K = 8, 4 warps: 1024-body blocks
 constexpr int kDefaultSymVariant = 0;   // K = 8, 8 warps: 2048-body blocks
@@ -636,6 +637,30 @@ bool plan_sym(int64_t n, int sm, int occ, int variant, int splits_req, int dists
         p_hi_req = p_hi_req / 2;   // a forced piece count too large for the design budget
     }
     if (best_p == 0) return false;
+
+    // Finer pieces for the 512- and 1024-body blocks from kSymFinerMinN
+    // bodies, in one pass: the wave model above counts whole waves, but
+    // several waves of smaller CTAs balance better across the SMs.
+    // Measured on GB300 (force call, us, model P -> 2P -> 3P):
+    //   16384: 115.4 / 112.1 / 125.9 (3P leaves pieces of 1 and 2 units)
+    //   20000: 168.3 / 160.4 / 157.2      45056: 750.9 / 715.8 / 697.5
+    //   65536: 1398 / 1365 / 1357        100000: 3469 / 3328 / 3268
+    //  163839: 8310 / 8232 / 8212   (2048-body blocks from 163840: +-0.5 %)
+    // so 3P where the pieces stay within 10 % of equal, else 2P.
+    if (splits_req <= 0 && variant != kDefaultSymVariant && n >= kSymFinerMinN) {
+        const int64_t groups0 = ceil_div(g.ndist, best_d);
+        const int64_t js0 = nbody::sym_group_jslots(static_cast<int>(g.nb), static_cast<int>(best_d));
+        const int64_t units = std::min<int64_t>(best_d, g.ndist) * g.spb;   // of the largest group
+        for (int64_t k : {3, 2}) {
+            const int64_t P2 = k * best_p;
+            if (P2 > std::min<int64_t>(kMaxSplits, units)) continue;
+            if (static_cast<double>(ceil_div(units, P2) * P2) > 1.1 * static_cast<double>(units))
+                continue;
+            if (groups0 * (P2 + js0) * rec > design || g.nb * P2 * groups0 > grid_cap) continue;
+            best_p = P2;
+            break;
+        }
+    }
 
     // execution within the workspace
     const int64_t P = best_p, D = best_d;
