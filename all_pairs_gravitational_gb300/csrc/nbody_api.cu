@@ -519,11 +519,14 @@ nbody::RowsLaunch rows_launch(const nbody_plan &plan) {
 // CUDA graphs: from 10240 bodies every shape below beats the tiled path
 // (54.5 against 57.6 us at 10240; 221 against 264 us at 24576), 512-body
 // blocks win up to about 45K bodies (better filled waves), 1024-body blocks
-// up to about 160K, and 2048-body blocks above (fewer partial slots); each
-// choice is within 4.5 % of the fastest shape at every size measured.
+// (with the finer pieces below) up to about 330K, and 2048-body blocks above
+// (fewer partial slots): 1024 against 2048, ms: 163840 bodies 8.21 / 8.39,
+// 262144 20.85 / 21.09, 393216 46.96 / 47.10, 524288 83.83 / 83.68, 2^20
+// 335.8 / 334.3.  Each choice is within 4.5 % of the fastest shape at every
+// size measured.
 constexpr int64_t kSymMinN = 10240;
 constexpr int64_t kSymMidN = 45056;     // from here 1024-body blocks
-constexpr int64_t kSymLargeN = 163840;  // from here 2048-body blocks
+constexpr int64_t kSymLargeN = 327680;  // from here 2048-body blocks
 constexpr int64_t kSymFinerMinN = 16384; // finer pieces for the smaller blocks from here
 constexpr int kSymSmallVariant = 2;     // K = 8, 2 warps: 512-body blocks
 constexpr int kSymMidVariant = 1;       // K = 8, 4 warps: 1024-body blocks
@@ -645,7 +648,7 @@ bool plan_sym(int64_t n, int sm, int occ, int variant, int splits_req, int dists
     //   16384: 115.4 / 112.1 / 125.9 (3P leaves pieces of 1 and 2 units)
     //   20000: 168.3 / 160.4 / 157.2      45056: 750.9 / 715.8 / 697.5
     //   65536: 1398 / 1365 / 1357        100000: 3469 / 3328 / 3268
-    //  163839: 8310 / 8232 / 8212   (2048-body blocks from 163840: +-0.5 %)
+    //  163839: 8310 / 8232 / 8212   (2048-body blocks: +-0.5 %)
     // so 3P where the pieces stay within 10 % of equal, else 2P.
     if (splits_req <= 0 && variant != kDefaultSymVariant && n >= kSymFinerMinN) {
         const int64_t groups0 = ceil_div(g.ndist, best_d);

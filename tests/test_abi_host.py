@@ -389,7 +389,7 @@ def test_symmetric_plan(lib, n, splits):
 
 
 @pytest.mark.parametrize("sm", [1, 148, 160, 264])
-@pytest.mark.parametrize("n", [10240, 45056, 163840, 1048576, 2097159])
+@pytest.mark.parametrize("n", [10240, 45056, 163840, 327680, 1048576, 2097159])
 @pytest.mark.parametrize("variant", [-1, 0, 1, 2])
 def test_symmetric_plan_other_gpus_and_variants(n, sm, variant):
     plan = apg.nbody_plan_forces(n, sm, path=apg.NBODY_PATH_SYMMETRIC, variant=variant)
@@ -508,7 +508,7 @@ def test_auto_path_choice():
         [7, 7, 4, 7]
     # the symmetric block size grows with n: 512, 1024, then 2048 bodies
     blocks = [apg.nbody_plan_forces(n, 152)["threads"] * apg.nbody_plan_forces(n, 152)["i_per_thread"]
-              for n in (10240, 45055, 45056, 163839, 163840, 1048576)]
+              for n in (10240, 45055, 45056, 327679, 327680, 1048576)]
     assert blocks == [512, 512, 1024, 1024, 2048, 2048]
     assert apg.nbody_plan_forces(1048576, 152)["path"] == apg.NBODY_PATH_SYMMETRIC
     with pytest.raises(apg.NbodyError):

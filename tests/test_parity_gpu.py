@@ -479,10 +479,10 @@ def test_symmetric_path_partials_past_2_34_bytes():
     test_symmetric_path_counts_every_pair_once(n, 0)
 
 
-@pytest.mark.parametrize("n", [10239, 10240, 45055, 45056, 163839, 163840])
+@pytest.mark.parametrize("n", [10239, 10240, 45055, 45056, 327679, 327680])
 def test_planner_switch_points(n):
-    """Either side of each automatic switch: tiled to symmetric at 10240,
-    512- to 1024-body blocks at 45056, 1024- to 2048-body blocks at 163840."""
+    """Either side of each automatic switch: row-split to symmetric at 10240,
+    512- to 1024-body blocks at 45056, 1024- to 2048-body blocks at 327680."""
     w = W.clumps(n, seed=n % 997)
     acc = gpu_forces(w.pos_mass, w.eps2)
     rows = np.unique(np.concatenate([sample_rows(n, 600, 11), np.arange(n - 64, n)]))
