@@ -269,8 +269,9 @@ def nbody_forces_workspace_bytes(n, eps2=1e-4, path=NBODY_PATH_AUTO, variant=-1,
 
 
 def nbody_forces_ts_ws(targets, sources, eps2, out=None, workspace=None, path=NBODY_PATH_AUTO,
-                       quantities=NBODY_QUANTITIES_ACC_POT, stream=None):
-    """nbody_forces_ts within a caller-owned workspace tensor."""
+                       quantities=NBODY_QUANTITIES_ACC_POT, stream=None, variant=-1, splits=0):
+    """nbody_forces_ts within a caller-owned workspace tensor (launch options
+    as nbody_forces_ex)."""
     import torch
     lib = load_library()
     _bodies(targets, "targets")
@@ -281,7 +282,7 @@ def nbody_forces_ts_ws(targets, sources, eps2, out=None, workspace=None, path=NB
         raise ValueError("targets, sources and out must be on the same device")
     ptr, nbytes = _workspace(workspace, targets.device, _ptr(out))
     size = ctypes.c_size_t(nbytes)
-    opts = _opts(path=path, quantities=quantities)
+    opts = _opts(path=path, variant=variant, splits=splits, quantities=quantities)
     with torch.cuda.device(targets.device):
         st = lib.nbody_forces_ts_ws(_ptr(targets), nt, _ptr(sources), ns,
                                     ctypes.c_float(float(eps2)), _ptr(out), ctypes.byref(opts),

@@ -535,6 +535,26 @@ def test_target_source_form(nt, ns):
     assert_parity(out.cpu().numpy(), oracle.forces_ts(t, s, eps2))
 
 
+@pytest.mark.parametrize("path,splits", [(1, 7), (1, 1), (4, 3)])
+def test_target_source_forced_launch_options(path, splits):
+    """The target/source call within a workspace, with a forced path and
+    piece count: tiled pieces through the workspace and the row-split path's
+    pieces in shared memory."""
+    t, s = _ts_bodies(3000, 9000, 41)
+    eps2 = np.float32(1e-3)
+    tt, st = torch.from_numpy(t).to(dev()), torch.from_numpy(s).to(dev())
+    plan = apg.nbody_plan_forces_ts(3000, 9000, sm_count_of_device(), path=path, splits=splits)
+    assert plan["path"] == path and plan["splits"] == splits
+    ws = torch.empty(max(16, plan["scratch_bytes"]), dtype=torch.uint8, device=dev())
+    out = apg.nbody_forces_ts_ws(tt, st, float(eps2), workspace=ws, path=path, splits=splits)
+    torch.cuda.synchronize()
+    assert_parity(out.cpu().numpy(), oracle.forces_ts(t, s, eps2))
+
+
+def sm_count_of_device():
+    return torch.cuda.get_device_properties(dev()).multi_processor_count
+
+
 def test_target_source_golden_three_body():
     """The worked three-body example through the target/source form: target 0
     against the three bodies."""
