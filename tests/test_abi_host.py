@@ -521,6 +521,23 @@ def test_auto_path_choice():
         apg.nbody_plan_forces(20000, 152, quantities=2)
 
 
+def test_symmetric_finer_pieces():
+    """From 16384 bodies the 512- and 1024-body blocks take 3x (else 2x) the
+    wave model's pieces in one pass, pieces within 10 % of equal; the
+    2048-body blocks and smaller n keep the model's count."""
+    picks = {n: apg.nbody_plan_forces(n, 152)["splits"]
+             for n in (12000, 16384, 20000, 45056, 65536, 100000, 200003, 1048576)}
+    assert picks == {12000: 35, 16384: 68, 20000: 84, 45056: 39, 65536: 57, 100000: 18,
+                     200003: 102, 1048576: 16}
+    for n in (16384, 20000, 30000, 45055, 45056, 65536, 100000, 163839, 200003):
+        plan = apg.nbody_plan_forces(n, 152)
+        nb, d, p = plan["num_iblocks"], plan["dists"], plan["splits"]
+        spb = plan["threads"] * plan["i_per_thread"] // plan["tile"]
+        units = min(d, _ndist(nb)) * spb
+        assert plan["passes"] == 1 and -(-units // p) * p <= 1.1 * units
+        _covers(plan, n)
+
+
 def test_acceleration_only_plans_like_the_default():
     for n in (1000, 8192, 20011, 1048576):
         a = apg.nbody_plan_forces(n, 152)
