@@ -5,7 +5,8 @@ The compute path lives in ``libnbody.so`` (hand-written sm_103a CUDA, see
 ``workloads`` draws the seeded synthetic bodies the tests and the benchmark
 use.
 """
-from ._binding import (EXPORTS, LIB_PATH, NBODY_DEFAULT_WORKSPACE_BYTES, NBODY_NOALLOC_MAX_N,
+from ._binding import (EXPORTS, LIB_PATH, NBODY_DEFAULT_WORKSPACE_BYTES, NBODY_MIN_EPS2,
+                       NBODY_NOALLOC_MAX_N,
                        NBODY_PATH_AUTO, NBODY_PATH_CLUSTER, NBODY_PATH_ROWS, NBODY_PATH_SYMMETRIC,
                        NBODY_PATH_TILED, NBODY_POOL_KEEP_BYTES, NBODY_PRECISION_COMPENSATED,
                        NBODY_PRECISION_DEFAULT, NBODY_QUANTITIES_ACC, NBODY_QUANTITIES_ACC_POT,
@@ -17,7 +18,7 @@ from ._binding import (EXPORTS, LIB_PATH, NBODY_DEFAULT_WORKSPACE_BYTES, NBODY_N
                        nbody_simulate, nbody_simulate_workspace_bytes, nbody_simulate_ws,
                        nbody_status_string)
 
-__all__ = ["EXPORTS", "LIB_PATH", "NBODY_DEFAULT_WORKSPACE_BYTES", "NBODY_NOALLOC_MAX_N",
+__all__ = ["EXPORTS", "LIB_PATH", "NBODY_DEFAULT_WORKSPACE_BYTES", "NBODY_MIN_EPS2", "NBODY_NOALLOC_MAX_N",
            "NBODY_PATH_AUTO", "NBODY_PATH_CLUSTER", "NBODY_PATH_ROWS", "NBODY_PATH_SYMMETRIC", "NBODY_PATH_TILED",
            "NBODY_POOL_KEEP_BYTES", "NBODY_PRECISION_COMPENSATED", "NBODY_PRECISION_DEFAULT",
            "NBODY_QUANTITIES_ACC", "NBODY_QUANTITIES_ACC_POT", "NbodyError", "load_library",

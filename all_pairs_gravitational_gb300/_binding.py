@@ -25,6 +25,7 @@ NBODY_QUANTITIES_ACC_POT = 0
 NBODY_QUANTITIES_ACC = 1
 NBODY_DEFAULT_WORKSPACE_BYTES = 1000000000
 NBODY_POOL_KEEP_BYTES = 64 << 20
+NBODY_MIN_EPS2 = 1.0e-25      # smallest accepted eps^2 (as the header's)
 
 STATUS_NAMES = {
     0: "NBODY_OK", 1: "NBODY_ERR_INVALID_ARG", 2: "NBODY_ERR_MISALIGNED", 3: "NBODY_ERR_ALIAS",

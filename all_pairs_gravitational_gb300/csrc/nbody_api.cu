@@ -38,7 +38,7 @@ nbody_status check_n(int64_t n) {
     return (n < 0 || n > INT32_MAX) ? NBODY_ERR_INVALID_ARG : NBODY_OK;
 }
 
-bool eps2_ok(float eps2) { return std::isfinite(eps2) && eps2 >= FLT_MIN; }
+bool eps2_ok(float eps2) { return std::isfinite(eps2) && eps2 >= NBODY_MIN_EPS2; }
 
 nbody_status check_forces(const float *pm, int64_t n, float eps2, const float *acc) {
     if (check_n(n) != NBODY_OK) return NBODY_ERR_INVALID_ARG;

@@ -99,7 +99,7 @@ extern "C" nbody_status nbody_forces_noalloc(const float *pos_mass, int64_t n, f
     if (n < 0 || n > INT32_MAX) return NBODY_ERR_INVALID_ARG;
     if (n == 0) return NBODY_OK;
     if (pos_mass == nullptr || acc_pot == nullptr) return NBODY_ERR_INVALID_ARG;
-    if (!std::isfinite(eps2) || !(eps2 >= FLT_MIN)) return NBODY_ERR_INVALID_ARG;
+    if (!std::isfinite(eps2) || !(eps2 >= NBODY_MIN_EPS2)) return NBODY_ERR_INVALID_ARG;
     if (!aligned16(pos_mass) || !aligned16(acc_pot)) return NBODY_ERR_MISALIGNED;
     if (overlap(pos_mass, acc_pot, 16 * n)) return NBODY_ERR_ALIAS;
     if (n > NBODY_NOALLOC_MAX_N) return NBODY_ERR_TOO_LARGE;

@@ -78,13 +78,21 @@ typedef enum nbody_status {
 /* Freed pool memory kept for the next call across synchronisations. */
 #define NBODY_POOL_KEEP_BYTES (64LL << 20)
 
+/* Smallest accepted eps^2.  The branch-free self term (and any two bodies at
+ * the same point) evaluates m * (eps^2)^(-3/2) * 0, which is 0 only while
+ * m * (eps^2)^(-3/2) is finite in fp32: here (eps^2)^(-3/2) = 3.2e37, so
+ * masses up to about 10 are safe; with larger masses eps^2 must grow with
+ * them (m * (eps^2)^(-3/2) < 3.4e38), or those accelerations are NaN. */
+#define NBODY_MIN_EPS2 1.0e-25f
+
 /*
  * nbody_forces -- acceleration and potential of every body from every body.
  *
  *   pos_mass : device, n records (x, y, z, m), fp32, 16-byte aligned.  Read only.
  *   n        : number of bodies.
- *   eps2     : softening eps^2 (not eps), fp32.  Must be finite and >= FLT_MIN
- *              (the branch-free self term needs |r|^2 + eps^2 > 0).
+ *   eps2     : softening eps^2 (not eps), fp32.  Must be finite and
+ *              >= NBODY_MIN_EPS2 (the branch-free self term needs
+ *              |r|^2 + eps^2 > 0 and m (eps^2)^(-3/2) finite; see there).
  *   acc_pot  : device, n records (ax, ay, az, p), fp32, 16-byte aligned.
  *              Written in full; must not overlap pos_mass.
  *   stream   : CUDA stream of the launch.

@@ -33,6 +33,11 @@ def _declared_functions():
 
 def test_header_and_binding_agree():
     assert _declared_functions() == sorted(apg.EXPORTS)
+    header = open(HEADER).read()
+    assert re.search(r"#define NBODY_MIN_EPS2 1\.0e-25f", header)
+    assert apg.NBODY_MIN_EPS2 == 1.0e-25
+    # the self term's m (eps^2)^(-3/2) stays finite in fp32 for m up to 10
+    assert 10.0 * np.float32(apg.NBODY_MIN_EPS2) ** -1.5 < np.finfo(np.float32).max
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -62,7 +67,8 @@ def test_forces_argument_checks(lib):
     assert _forces(lib, P, 2 ** 31, 1e-4, P + 2 ** 36) == 1
     assert _forces(lib, 0, 10, 1e-4, P) == 1                         # null input
     assert _forces(lib, P, 10, 1e-4, 0) == 1                         # null output
-    for bad in (0.0, -1e-4, float("nan"), float("inf"), 1e-40):      # 1e-40 is subnormal
+    for bad in (0.0, -1e-4, float("nan"), float("inf"), 1e-40,       # 1e-40 is subnormal
+                1.17549435e-38, 1e-26, 9.9e-26):   # (eps2)^(-3/2) overflows fp32 below 2.05e-26
         assert _forces(lib, P, 10, bad, P + 4096) == 1, bad
     assert _forces(lib, P + 4, 10, 1e-4, P + 4096) == 2              # misaligned input
     assert _forces(lib, P, 10, 1e-4, P + 4104) == 2                  # misaligned output

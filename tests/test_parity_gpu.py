@@ -215,6 +215,24 @@ def test_single_body_self_term():
     assert out[0, 3] == pytest.approx(-8.0, rel=1e-6)
 
 
+@pytest.mark.parametrize("path", [1, 2, 3, 4])
+def test_smallest_accepted_softening(path):
+    """eps^2 = NBODY_MIN_EPS2: the self term m (eps^2)^(-3/2) * 0 stays 0
+    (finite in fp32 for masses up to 10), on every path; a lone body has
+    a = 0 and p = -m / eps."""
+    eps2 = apg.NBODY_MIN_EPS2
+    one = gpu_forces(np.array([[0.25, -0.5, 0.75, 10.0]], np.float32), eps2,
+                     path=path if path != 3 else 0)
+    assert np.all(one[0, :3] == 0.0)
+    np.testing.assert_allclose(one[0, 3], -10.0 / np.sqrt(np.float64(np.float32(eps2))), rtol=1e-6)
+    w = W.cube(5003, seed=61)
+    pm = w.pos_mass.copy()
+    pm[:, 3] = np.random.default_rng(5).uniform(0.1, 10.0, w.n).astype(np.float32)
+    got = gpu_forces(pm, eps2, path=path)
+    assert np.all(np.isfinite(got))
+    assert_parity(got, oracle.forces(pm, np.float32(eps2)))
+
+
 def test_two_body_closed_form():
     pm = np.array([[0, 0, 0, 1], [4, 0, 0, 2]], np.float32)
     out = gpu_forces(pm, 9.0).astype(np.float64)
